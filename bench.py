@@ -1,0 +1,491 @@
+"""Benchmark of the GB300 reduce / scan library.
+
+One step = the whole-array mapreduce workload at n = 1e8: the f32
+uniform[-1,1) abs2 sum, and the i64 uniform[-2^20, 2^20] sum and max, each
+into a one-element device array through the C ABI (ak_reduce). Inputs are
+400 / 800 MB, larger than the 129 MB L2, and the calls are ordered so that no
+call follows one over the same array. The metric is achieved HBM GB/s
+(algorithmic bytes read + written / GPU time) and its fraction of the
+measured HBM copy bandwidth; the JSON line also carries microseconds per
+call, the per-workload kernel numbers of the other reduce / dims / scan
+workloads (L2 flushed before every timed call), the end-to-end number with
+host buffers, and the sequential CPU oracle timed on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--no-configs] [--small]
+Under torchrun every rank runs the same workload on its own GPU (independent
+replicas: the workload has no exchange step); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+N_BIG = 10**8
+METRIC = "achieved HBM GB/s and % of GB300 peak; us/call for reduce/scan at 1e8 fp32"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _rank_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ak_clocks_{os.getpid()}.csv")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        busy = [s for s in sm if mx and s > 0.3 * max(mx)]
+        return {"sm_mhz": statistics.median(busy or sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def _traffic_from_profile(kernel_hash: str):
+    """DRAM bytes per launch of the whole-array first pass from the committed
+    ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "reduce_pass1_1e8.md")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    vals = {}
+    for ln in lines:
+        if ":" in ln and ln.strip().startswith("- "):
+            k, v = ln.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256") != kernel_hash:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_f32_abs2"])
+    except (KeyError, ValueError):
+        return None
+
+
+def _kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("reduce.cu", "ak_common.cuh", "ak_types.cuh"):
+        with open(os.path.join(ROOT, "mapreduce_prefix_scan_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _flush_l2(buf):
+    buf.zero_()
+
+
+def _time_call(fn, reps, flush_buf, torch):
+    """Median / min microseconds of fn() with the L2 flushed before each call."""
+    s = torch.cuda.current_stream()
+    ts = []
+    for _ in range(3):
+        fn()
+    for _ in range(reps):
+        _flush_l2(flush_buf)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        fn()
+        e1.record(s)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(ts), min(ts)
+
+
+def _configs(ak, torch, dev, peak, flush_buf, reps):
+    """Per-workload kernel numbers (L2 flushed before every timed call)."""
+    out = {}
+
+    def rec(name, fn, nbytes, check=None):
+        med, mn = _time_call(fn, reps, flush_buf, torch)
+        out[name] = {"us_median": round(med, 2), "us_min": round(mn, 2), "bytes": nbytes,
+                     "gbs": round(nbytes / med / 1e3, 1), "frac": round(nbytes / med / 1e3 / peak, 3)}
+
+    # 1e6 f32 / i32 sums (latency-bound)
+    x = torch.from_numpy(synth.uniform_f32_pm1(10**6, 0, 0)).to(dev)
+    xi = torch.from_numpy(synth.uniform_int(10**6, -1000, 1000, np.int32, 0, 1)).to(dev)
+    r = torch.empty(1, device=dev)
+    ri = torch.empty(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    rec("sum_f32_1e6_device", lambda: ak.ak_reduce(x, dst=r, init=0.0, workspace=ws), 4 * 10**6 + 4)
+    rec("sum_f32_1e6_host", lambda: ak.ak_reduce(x, to_host=True, init=0.0, workspace=ws), 4 * 10**6 + 4)
+    rec("sum_i32_1e6_device", lambda: ak.ak_reduce(xi, dst=ri, workspace=ws), 4 * 10**6 + 4)
+    del x, xi
+    # strided dims=2 reductions
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+    for name, shape, kind in [("dims2_3072x2048_bf16", (3072, 2048), "bf16"),
+                              ("dims2_768x1024x8_bf16", (768, 1024, 8), "bf16"),
+                              ("dims2_768x1024x8_f32", (768, 1024, 8), "f32"),
+                              ("dims2_64x4096x32_f32", (64, 4096, 32), "f32"),
+                              ("dims2_8192x8192_f32", (8192, 8192), "f32")]:
+        n = int(np.prod(shape))
+        if kind == "bf16":
+            a = torch.from_numpy(synth.normal_bf16_bits(n, 0, 40).view(np.int16)).view(torch.bfloat16)
+        else:
+            a = torch.from_numpy(synth.normal_f32(n, 0, 40))
+        a = a.reshape(tuple(reversed(shape))).to(dev)
+        nout = n // shape[1]
+        esz = 2 if kind == "bf16" else 4
+        dst = torch.empty(nout, dtype=a.dtype, device=dev)
+        rec(name, lambda a=a, dst=dst, shape=shape: ak.ak_reduce_dims(a, [1], shape=shape, dst=dst, workspace=ws),
+            n * esz + nout * esz)
+        del a
+    # scans
+    a = torch.from_numpy(synth.uniform_f64_01(N_BIG, 0, 60)).to(dev)
+    y = torch.empty_like(a)
+    ws_s = torch.empty(ak.ak_accumulate_workspace_size([N_BIG], -1, "f64", "f64"), dtype=torch.uint8, device=dev)
+    rec("cumsum_f64_1e8", lambda: ak.ak_accumulate(a, dst=y, workspace=ws_s), 16 * N_BIG)
+    del a, y
+    a = torch.from_numpy(synth.normal_f32(10**7, 0, 61)).to(dev)
+    y = torch.empty_like(a)
+    o = ak.make_opts(no_neutral=True)
+    ws_s = torch.empty(ak.ak_accumulate_workspace_size([10**7], -1, "f32", "f32", "max", o), dtype=torch.uint8,
+                       device=dev)
+    rec("accumulate_max_optional_f32_1e7", lambda: ak.ak_accumulate(a, dst=y, op="max", opts=o, workspace=ws_s),
+        8 * 10**7)
+    del a, y
+    a = torch.from_numpy(synth.normal_f32(4096 * 4096, 0, 62)).reshape(4096, 4096).to(dev)
+    y = torch.empty_like(a)
+    ws_s = torch.empty(256, dtype=torch.uint8, device=dev)
+    rec("cumsum_dims1_4096x4096_f32", lambda: ak.ak_accumulate(a, dst=y, dim=0, workspace=ws_s), 8 * 4096 * 4096)
+    del a, y
+    a = torch.from_numpy(synth.mat2_modp(10**7, 0, 63)).to(dev)
+    y = torch.empty_like(a)
+    ws_s = torch.empty(ak.ak_accumulate_workspace_size([10**7], -1, "mat2", "mat2", "matmul"), dtype=torch.uint8,
+                       device=dev)
+    rec("prefix_matmul_modp_1e7", lambda: ak.ak_accumulate(a, dst=y, op="matmul", elem="mat2", workspace=ws_s),
+        32 * 10**7)
+    del a, y
+    a = torch.from_numpy(synth.mat2_modp(1024 * 8192, 0, 64)).reshape(8192, 1024, 4).to(dev)
+    y = torch.empty_like(a)
+    ws_s = torch.empty(256, dtype=torch.uint8, device=dev)
+    rec("prefix_matmul_modp_dims1_1024x8192", lambda: ak.ak_accumulate(a, dst=y, op="matmul", elem="mat2", dim=0,
+                                                                       workspace=ws_s), 32 * 1024 * 8192)
+    del a, y
+    return out
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import mapreduce_prefix_scan_gb300 as ak
+    from mapreduce_prefix_scan_gb300 import _abi
+
+    rank, world, local = _rank_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peak, peak_kind = _peaks()
+    n = 10**6 if args.small else N_BIG
+
+    # inputs (generated on the host, copied once; resident when timing starts)
+    xf_h = torch.from_numpy(synth.uniform_f32_pm1(n, 0, 2)).pin_memory()
+    xi_h = torch.from_numpy(synth.uniform_int(n, -(2**20), 2**20, np.int64, 0, 3)).pin_memory()
+    xf = xf_h.to(dev)
+    xi = xi_h.to(dev)
+    rf = torch.empty(1, dtype=torch.float32, device=dev)
+    rs = torch.empty(1, dtype=torch.int64, device=dev)
+    rm = torch.empty(1, dtype=torch.int64, device=dev)
+    L = ak.lib()
+    wsz = max(ak.ak_reduce_workspace_size(n, "f32", "f32"), ak.ak_reduce_workspace_size(n, "i64", "i64"))
+    ws = torch.empty(wsz, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    D, M, O, S = _abi.DTYPES, _abi.MAPS, _abi.OPS, _abi.STORES
+
+    # the three calls of a step, through the C ABI with prepared arguments
+    calls = [
+        ("i64_sum", lambda: L.ak_reduce(xi.data_ptr(), n, D["i64"], M["identity"], O["add"], D["i64"], D["i64"], None,
+                                        S["overwrite"], rs.data_ptr(), None, ws.data_ptr(), wsz, None, sp), 8 * n + 8),
+        ("f32_abs2_sum", lambda: L.ak_reduce(xf.data_ptr(), n, D["f32"], M["abs2"], O["add"], D["f32"], D["f32"],
+                                             None, S["overwrite"], rf.data_ptr(), None, ws.data_ptr(), wsz, None, sp),
+         4 * n + 4),
+        ("i64_max", lambda: L.ak_reduce(xi.data_ptr(), n, D["i64"], M["identity"], O["max"], D["i64"], D["i64"], None,
+                                        S["overwrite"], rm.data_ptr(), None, ws.data_ptr(), wsz, None, sp), 8 * n + 8),
+    ]
+    step_bytes = sum(c[2] for c in calls)
+
+    def step(evs=None):
+        for k, (_, fn, _) in enumerate(calls):
+            if evs is not None:
+                evs[k][0].record(stream)
+            st = fn()
+            if evs is not None:
+                evs[k][1].record(stream)
+            if st != 0:
+                raise RuntimeError(f"ak_reduce failed: {ak.ak_status_string(st)}")
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    # correctness guard on the timed workload (cheap integer checks)
+    assert rs.item() == int(xi_h.sum().item()) and rm.item() == int(xi_h.max().item())
+
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = ak.ak_kernel_launch_count()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_end()
+    if world > 1:
+        dist.barrier()
+    launches = ak.ak_kernel_launch_count() - launches0
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    per_call_us = {}
+    for k, (name, _, _) in enumerate(calls):
+        per_call_us[name] = statistics.median([evs[i][k][0].elapsed_time(evs[i][k][1]) * 1e3 for i in range(args.steps)])
+    call_us_total = sum(per_call_us[c[0]] for c in calls)
+    achieved = step_bytes / call_us_total / 1e3  # GB/s over the ak_reduce calls
+    value = world * step_bytes * args.steps / (ms * 1e-3) / 1e9
+
+    # end to end: host buffers, H2D inside the timed region, D2H of the results
+    e2e_steps = 3 if not args.small else 10
+    hs = torch.empty(1, dtype=torch.int64).pin_memory()
+    hm = torch.empty(1, dtype=torch.int64).pin_memory()
+    hf = torch.empty(1, dtype=torch.float32).pin_memory()
+    xf_d2 = torch.empty_like(xf)
+    xi_d2 = torch.empty_like(xi)
+
+    def e2e_step():
+        xi_d2.copy_(xi_h, non_blocking=True)
+        xf_d2.copy_(xf_h, non_blocking=True)
+        ak.ak_reduce(xi_d2, dst=rs, workspace=ws)
+        ak.ak_reduce(xf_d2, f="abs2", dst=rf, workspace=ws)
+        ak.ak_reduce(xi_d2, op="max", dst=rm, workspace=ws)
+        hs.copy_(rs, non_blocking=True)
+        hf.copy_(rf, non_blocking=True)
+        hm.copy_(rm, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e = {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": int(xi_h.numel() * 8 + xf_h.numel() * 4), "d2h_bytes_per_step": 8 + 8 + 4,
+           "ms_per_step": round(e2e_ms, 3)}
+    del xf_d2, xi_d2
+
+    configs = None
+    if not args.no_configs and not args.small and rank == 0:
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        del xf, xi
+        torch.cuda.empty_cache()
+        configs = _configs(ak, torch, dev, peak, flush, args.config_reps)
+
+    cpu = None
+    if rank == 0:
+        cpu = _cpu_baseline(xf_h.numpy(), xi_h.numpy(), budget_s=args.cpu_budget)
+
+    if rank == 0:
+        khash = _kernel_source_hash()
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32,i64", "data": "synthetic",
+            "config": {"workload": f"whole-array mapreduce n={n}: f32 uniform[-1,1) abs2 sum, i64 "
+                                   "uniform[-2^20,2^20] sum and max, each into a one-element device array",
+                       "n": n, "calls_per_step": 3, "bytes_per_step": step_bytes,
+                       "l2": "inputs larger than L2 (400/800 MB); no call follows one over the same array",
+                       "parallelism": f"replicas x{world}"},
+            "us_per_call": {k: round(v, 2) for k, v in per_call_us.items()},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": _traffic_from_profile(khash),
+                         "kernel": "ak_reduce (first pass + one-block finish) on n=1e8",
+                         "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                         else "fallback 6.8 TB/s"},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": int(launches),
+            "clocks": clk,
+            "kernel_source": khash,
+        }
+        if configs is not None:
+            line["configs"] = configs
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline, and the reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_step(xf: np.ndarray, xi: np.ndarray):
+    import oracle
+
+    t = time.perf_counter()
+    oracle.reduce(xi, "i64", op="add")
+    oracle.reduce(xf, "f32", map="abs2")
+    oracle.reduce(xi, "i64", op="max")
+    return time.perf_counter() - t
+
+
+def _cpu_baseline(xf: np.ndarray, xi: np.ndarray, budget_s: float = 20.0):
+    import oracle
+
+    oracle.lib()
+    # calibrate on 1e6 elements, then run as much of the workload as fits the budget
+    t = _oracle_step(xf[: 10**6], xi[: 10**6])
+    m = int(min(xf.size, max(10**6, budget_s / max(t, 1e-9) * 10**6 / 3)))
+    passes = 0
+    total = 0.0
+    while passes < 3 and (passes == 0 or total < budget_s / 3):
+        total += _oracle_step(xf[:m], xi[:m])
+        passes += 1
+    nbytes = passes * (4 * m + 16 * m)
+    return {"value": round(nbytes / total / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{passes} pass(es) of the step over the first {m} elements of each array "
+                      f"(f32 abs2 sum, i64 sum, i64 max; sequential C, f64 / exact integer)",
+            "us_per_step_full": round(total / passes * (xf.size / m) * 1e6, 1)}
+
+
+def run_reference(args):
+    rank, world, _ = _rank_env()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.lib()
+    n = N_BIG if not args.small else 10**6
+    # bounded sample: the whole --steps/--warmup run fits in about a minute
+    probe = 10**6
+    xf = synth.uniform_f32_pm1(probe, 0, 2)
+    xi = synth.uniform_int(probe, -(2**20), 2**20, np.int64, 0, 3)
+    t = _oracle_step(xf, xi)
+    per_step_budget = 60.0 / max(1, args.steps + args.warmup)
+    m = int(max(10**4, min(n, per_step_budget / max(t, 1e-9) * probe)))
+    xf = synth.uniform_f32_pm1(m, 0, 2)
+    xi = synth.uniform_int(m, -(2**20), 2**20, np.int64, 0, 3)
+    for _ in range(args.warmup):
+        _oracle_step(xf, xi)
+    total = 0.0
+    for _ in range(args.steps):
+        total += _oracle_step(xf, xi)
+    nbytes = args.steps * (4 * m + 4 + 2 * (8 * m + 8))
+    value = nbytes / total / 1e9
+    sample = f"first {m} of the {n} elements of each array per step"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64,i64",
+            "data": "synthetic",
+            "config": {"workload": f"whole-array mapreduce n={n}: f32 uniform[-1,1) abs2 sum, i64 "
+                                   "uniform[-2^20,2^20] sum and max (sequential CPU oracle)", "n": n},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload kernel numbers")
+    ap.add_argument("--config-reps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--small", action="store_true", help="n = 1e6 (for profiling captures)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

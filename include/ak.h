@@ -1,0 +1,232 @@
+/*
+ * ak.h -- C ABI of the GB300 (sm_103a) device-wide reduce / prefix-scan library.
+ *
+ * Three operations, as stated in the AcceleratedKernels.jl pull requests
+ * this library re-designs for GB300:
+ *
+ *   ak_reduce       whole-array mapreduce(f, op, A) into a host scalar or a
+ *                   one-element device array ("Finish whole-array reductions
+ *                   on the device", PR #139, sections "What changes" and
+ *                   "Compatibility");
+ *   ak_reduce_dims  mapreducedim!(f, op, R, A) over a set of dimensions of a
+ *                   dense column-major array, e.g. sum(x; dims=2) of a matrix
+ *                   or of the middle dimension of a 3-d array (strided
+ *                   reduction PR #176, first two lists);
+ *   ak_accumulate   accumulate!(op, dst, src) / cumsum: the inclusive scan of
+ *                   the whole array or along one dimension, including
+ *                   operators with no neutral element and non-commutative
+ *                   ones (tile-scan PR #202, first paragraph and paragraph
+ *                   "Alternatives").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers. Arrays (src, dst, workspace) are DEVICE pointers to memory of the
+ *   current CUDA device; init and dst_host are HOST pointers. The caller owns
+ *   every buffer; the library allocates no device memory.
+ * Layout. Arrays are dense and column-major: element (i1, i2, ..., id) of a
+ *   shape (n1, ..., nd) sits at i1 + n1*(i2 + n2*(i3 + ...)) (0-based). This
+ *   is the memory of a contiguous row-major tensor of the reversed shape.
+ *   Dimensions are numbered from 0 (Julia's dims=2 is dimension 1 here).
+ * Element types (ak_dtype). AK_BF16 is the bfloat16 bit pattern; AK_MAT2_MODP
+ *   is a 2x2 matrix over Z/pZ, p = 2^31 - 1, stored as four uint32 entries in
+ *   column-major order (a11, a21, a12, a22), each in [0, p); its only operator
+ *   is AK_OP_MATMUL_MODP, the product mod p, with the left operand first.
+ * Types of a call. `in` is the element type of src; `acc` the accumulator in
+ *   which f is applied and op folds; `out` the type stored. Supported
+ *   (in -> acc -> out): F32->F32->F32, F32->F64->{F64,F32}, F64->F64->F64,
+ *   BF16->F32->{BF16,F32}, I32->I32->I32, I32->I64->I64, I64->I64->I64,
+ *   MAT2->MAT2->MAT2. f32 -> bf16 and f64 -> f32 stores round to nearest
+ *   even; integer accumulators wrap modulo 2^32 / 2^64.
+ * Order. Results equal the left-to-right fold up to the rounding of a
+ *   different association tree; non-commutative operators keep the element
+ *   order exactly. max / min follow Julia: NaN wins (returned as the
+ *   canonical quiet NaN) and +0.0 > -0.0.
+ * init. A host pointer to ONE value of the accumulator type, applied exactly
+ *   once, leftmost: op(init, ...).
+ * Asynchrony. Calls enqueue work on `stream` (a cudaStream_t, NULL = legacy
+ *   default stream) and return without waiting, except where stated. Calls
+ *   that share a workspace must be ordered on one stream.
+ * Workspace. A device buffer of at least the size the matching
+ *   *_workspace_size function reports for the same arguments (16-byte
+ *   aligned). Its contents on entry are arbitrary: no clearing is needed
+ *   between calls.
+ * Errors. Every call returns an ak_status. Arguments are validated before
+ *   anything is launched, so invalid calls have no effect on the device.
+ *   AK_ERR_CUDA keeps the CUDA error, readable with ak_last_cuda_error().
+ */
+#ifndef AK_H
+#define AK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ak_status {
+    AK_OK = 0,
+    AK_ERR_INVALID_ARG = 1,   /* bad pointer, size, enum, dims or store mode */
+    AK_ERR_UNSUPPORTED = 2,   /* valid but unsupported type / op / map combination */
+    AK_ERR_WORKSPACE = 3,     /* workspace missing, too small or misaligned */
+    AK_ERR_EMPTY_NO_INIT = 4, /* empty reduction, no init and no neutral element */
+    AK_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+    AK_ERR_TIMEOUT = 6        /* a bounded device-side wait ran out (scan look-back) */
+} ak_status;
+
+typedef enum ak_dtype {
+    AK_F32 = 0,
+    AK_F64 = 1,
+    AK_BF16 = 2,
+    AK_I32 = 3,
+    AK_I64 = 4,
+    AK_MAT2_MODP = 5
+} ak_dtype;
+
+/* f, applied to each element in the accumulator type before op. */
+typedef enum ak_map { AK_MAP_IDENTITY = 0, AK_MAP_ABS = 1, AK_MAP_ABS2 = 2 } ak_map;
+
+typedef enum ak_op {
+    AK_OP_ADD = 0,
+    AK_OP_MUL = 1,
+    AK_OP_MAX = 2,
+    AK_OP_MIN = 3,
+    AK_OP_MATMUL_MODP = 4
+} ak_op;
+
+/* How a reduction's result r is stored into R (PR #139, "What changes": the
+ * last pass applies init, folds into R's previous value, or writes):
+ *   AK_STORE_OVERWRITE  R = r
+ *   AK_STORE_INIT       R = op(init, r)    (init required)
+ *   AK_STORE_FOLD       R = op(R_old, r)   (R_old converted to acc first) */
+typedef enum ak_store { AK_STORE_OVERWRITE = 0, AK_STORE_INIT = 1, AK_STORE_FOLD = 2 } ak_store;
+
+/* Kernel shape of a strided dims reduction (PR #176, item 1): one thread per
+ * output, one pass over tiles of outputs, or tiles of outputs with the
+ * reduction split across blocks and a second pass. AUTO chooses by the
+ * number of outputs versus the reduction length. */
+typedef enum ak_dims_shape {
+    AK_SHAPE_AUTO = 0,
+    AK_SHAPE_THREAD = 1,
+    AK_SHAPE_TILED = 2,
+    AK_SHAPE_COLUMNS = 3
+} ak_dims_shape;
+
+/* Options; pass NULL for defaults or fill with ak_opts_default(). */
+typedef struct ak_opts {
+    int32_t no_neutral;       /* 1: treat op as having no neutral element; partial results
+                                 carry an Optional flag (e.g. 8 bytes for a Float32 acc) */
+    int32_t target_blocks;    /* whole-array first pass / persistent scan grid; 0 = auto */
+    int32_t items_per_thread; /* scan run length / reduce loads in flight; 0 = auto */
+    int32_t dims_shape;       /* ak_dims_shape */
+    int32_t check;            /* 1: synchronize `stream` before returning and report
+                                 device-side failures (AK_ERR_TIMEOUT) */
+    int32_t reserved0;
+    int64_t wait_limit_ns;    /* bound of each device-side wait of the scan; 0 = 1 s */
+    int64_t debug_skip_publish_tile; /* fault injection for tests: the scan tile with this
+                                 index never publishes its state, so its successors'
+                                 bounded waits run out; -1 = off */
+} ak_opts;
+
+void ak_opts_default(ak_opts* opts);
+
+const char* ak_status_string(ak_status status);
+/* Size in bytes of one element of the type; 0 for an invalid type. */
+size_t ak_dtype_size(ak_dtype dtype);
+/* The cudaError_t of the last AK_ERR_CUDA returned on this thread. */
+int ak_last_cuda_error(void);
+/* Number of kernels this library has launched in this process. */
+uint64_t ak_kernel_launch_count(void);
+
+/* ---------------------------------------------------------------------------
+ * ak_reduce: r = op(f(src[0]), f(src[1]), ..., f(src[n-1])), then stored by
+ * `mode` into a one-element device array and/or returned to the host.
+ * PR #139, "What changes": a first pass of a bounded number of blocks, each
+ * reducing its share of the input to one partial, and a one-block second
+ * pass that reduces the partials and performs the store; a small input takes
+ * one launch; for a host result the last pass stores the bare partial, which
+ * is copied back and finished on the host.
+ *
+ *   src        device, n elements of `in` (n == 0 allowed)
+ *   dst_dev    device, one element of `out`, or NULL
+ *   dst_host   host, one element of `out`, or NULL; when given the call
+ *              copies the result back and synchronizes `stream` (with
+ *              AK_STORE_FOLD, *dst_host holds R_old on entry, unless dst_dev
+ *              is also given, in which case R is the device element)
+ *   At least one of dst_dev / dst_host must be non-NULL.
+ * Empty input: AK_STORE_INIT stores init; AK_STORE_FOLD leaves R unchanged;
+ *   AK_STORE_OVERWRITE stores the neutral element of op (0 for +, 1 for *,
+ *   the identity matrix), or fails with AK_ERR_EMPTY_NO_INIT for max / min
+ *   and under no_neutral.
+ * ------------------------------------------------------------------------- */
+ak_status ak_reduce_workspace_size(int64_t n, ak_dtype in, ak_dtype acc, const ak_opts* opts,
+                                   size_t* bytes);
+ak_status ak_reduce(const void* src, int64_t n, ak_dtype in, ak_map f, ak_op op, ak_dtype acc,
+                    ak_dtype out, const void* init, ak_store mode, void* dst_dev, void* dst_host,
+                    void* workspace, size_t workspace_bytes, const ak_opts* opts, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * ak_reduce_dims: R[kept index] = op over the reduced dimensions of
+ * f(src[...]), folded in increasing column-major order of the reduced
+ * indices. PR #176: strided reductions into contiguous outputs take a 2-d
+ * block of outputs x reduction rows, split across blocks (plus a second
+ * pass) only when the outputs alone do not fill the device; the middle
+ * dimension of a 3-d array is handled as runs of contiguous outputs at the
+ * offsets of the other kept dimensions. PR #139: a reduction to a single
+ * output over one contiguous range takes the whole-array path.
+ *
+ *   ndim, shape   1 <= ndim <= 8, column-major extents (>= 0)
+ *   dims_mask     bit d set = dimension d is reduced (bits >= ndim invalid)
+ *   dst           device, dense column-major array of `out` with the shape of
+ *                 src where reduced extents are 1
+ * Empty reductions (a reduced extent is 0) follow ak_reduce's empty rules.
+ * ------------------------------------------------------------------------- */
+ak_status ak_reduce_dims_workspace_size(int ndim, const int64_t* shape, uint32_t dims_mask,
+                                        ak_dtype in, ak_dtype acc, const ak_opts* opts,
+                                        size_t* bytes);
+ak_status ak_reduce_dims(const void* src, int ndim, const int64_t* shape, uint32_t dims_mask,
+                         ak_dtype in, ak_map f, ak_op op, ak_dtype acc, ak_dtype out,
+                         const void* init, ak_store mode, void* dst, void* workspace,
+                         size_t workspace_bytes, const ak_opts* opts, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * ak_accumulate: inclusive scan. Along a line x_1, x_2, ...:
+ *   y_1 = op(init, x_1) (or x_1 without init), y_i = op(y_{i-1}, x_i).
+ * dim = -1 scans the whole array as one line (column-major order); dim = d
+ * scans every line along dimension d independently. PR #202, first
+ * paragraph: a tile is loaded striped, each thread scans its own run of
+ * consecutive elements, and the tile prefix is applied; runs are stored at an
+ * odd stride in shared memory. Tiles pass their prefixes on in a single pass
+ * (decoupled look-back, Merrill & Garland 2016); every wait is bounded.
+ *
+ *   src, dst      device, same shape; dst may equal src (in place) but must
+ *                 not otherwise overlap it
+ * A wait that runs out (only possible through debug_skip_publish_tile or a
+ * hardware fault) stops the kernel early; with opts->check set the call then
+ * returns AK_ERR_TIMEOUT and dst is unspecified.
+ * ------------------------------------------------------------------------- */
+ak_status ak_accumulate_workspace_size(int ndim, const int64_t* shape, int dim, ak_dtype in,
+                                       ak_dtype acc, ak_op op, const ak_opts* opts,
+                                       size_t* bytes);
+ak_status ak_accumulate(const void* src, void* dst, int ndim, const int64_t* shape, int dim,
+                        ak_dtype in, ak_op op, ak_dtype acc, ak_dtype out, const void* init,
+                        void* workspace, size_t workspace_bytes, const ak_opts* opts,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Shape selector of ak_reduce_dims, exposed for inspection and tests (pure
+ * host logic, no device needed). For a canonical strided problem of
+ * `inner` contiguous outputs, reduction length `red_len` at stride `inner`
+ * and `outer` output runs, elements of `elem_bytes` and vector width
+ * `vec_elems`, on a device of `sm_count` SMs, writes the chosen shape, the
+ * outputs per block along the contiguous dimension, the reduction rows per
+ * block and the split factor.
+ * ------------------------------------------------------------------------- */
+ak_status ak_dims_select(int64_t inner, int64_t red_len, int64_t outer, int elem_bytes,
+                         int vec_elems, int sm_count, int forced_shape, int32_t* shape_out,
+                         int32_t* tile_outputs, int32_t* row_groups, int32_t* split);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AK_H */

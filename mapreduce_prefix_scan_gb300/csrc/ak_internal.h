@@ -1,0 +1,224 @@
+// ak_internal.h -- host-side plumbing shared by the entry points: device
+// properties, call epochs, launch accounting, type dispatch and the call
+// descriptors handed from the validating front end (api.cu) to the kernel
+// launchers (reduce.cu, reduce_dims.cu, scan.cu).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cstring>
+#include <type_traits>
+#include <cuda_runtime.h>
+
+#include "../../include/ak.h"
+#include "ak_types.cuh"
+
+namespace ak {
+
+// ---------------------------------------------------------------------------
+// device properties (cached per device)
+// ---------------------------------------------------------------------------
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int max_smem_optin = 0;   // bytes per block with opt-in
+    int max_threads_per_sm = 0;
+    int l2_bytes = 0;
+};
+// Properties of the current device; returns false (and records the CUDA
+// error) when there is none.
+bool current_device(DeviceInfo* info);
+
+// ---------------------------------------------------------------------------
+// bookkeeping
+// ---------------------------------------------------------------------------
+// A process-unique 62-bit tag for one call: tile-state words written by
+// older calls (or arbitrary memory) never match it, so workspaces need no
+// clearing.
+uint64_t next_epoch();
+void count_launches(uint64_t k);
+ak_status cuda_fail(cudaError_t e);  // records e, returns AK_ERR_CUDA
+inline ak_status check_launch() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? AK_OK : cuda_fail(e);
+}
+
+// Workspace header (first 256 bytes of every workspace).
+struct WsHeader {
+    uint64_t error_word;  // (epoch << 8) | code, written by a kernel that gave up waiting
+    uint64_t pad[31];
+};
+constexpr size_t kWsHeader = 256;
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------
+// type dispatch
+// ---------------------------------------------------------------------------
+template <class T>
+struct Tag {
+    using type = T;
+};
+
+// Calls f(Tag<In>, Tag<Acc>, Tag<Out>) for the supported type triples.
+template <class F>
+ak_status dispatch_types(ak_dtype in, ak_dtype acc, ak_dtype out, F&& f) {
+#define AK_TRIPLE(I, A, O, TI, TA, TO) \
+    if (in == I && acc == A && out == O) return f(Tag<TI>{}, Tag<TA>{}, Tag<TO>{});
+    AK_TRIPLE(AK_F32, AK_F32, AK_F32, float, float, float)
+    AK_TRIPLE(AK_F32, AK_F64, AK_F64, float, double, double)
+    AK_TRIPLE(AK_F32, AK_F64, AK_F32, float, double, float)
+    AK_TRIPLE(AK_F64, AK_F64, AK_F64, double, double, double)
+    AK_TRIPLE(AK_BF16, AK_F32, AK_BF16, bf16, float, bf16)
+    AK_TRIPLE(AK_BF16, AK_F32, AK_F32, bf16, float, float)
+    AK_TRIPLE(AK_I32, AK_I32, AK_I32, int32_t, int32_t, int32_t)
+    AK_TRIPLE(AK_I32, AK_I64, AK_I64, int32_t, int64_t, int64_t)
+    AK_TRIPLE(AK_I64, AK_I64, AK_I64, int64_t, int64_t, int64_t)
+    AK_TRIPLE(AK_MAT2_MODP, AK_MAT2_MODP, AK_MAT2_MODP, Mat2, Mat2, Mat2)
+#undef AK_TRIPLE
+    return AK_ERR_UNSUPPORTED;
+}
+
+template <class Acc>
+constexpr bool is_mat2_v = std::is_same_v<Acc, Mat2>;
+
+// Calls f(Tag<Op>) for an operator valid on Acc.
+template <class Acc, class F>
+ak_status dispatch_op(ak_op op, F&& f) {
+    if constexpr (is_mat2_v<Acc>) {
+        if (op == AK_OP_MATMUL_MODP) return f(Tag<OpMatMul>{});
+        return AK_ERR_UNSUPPORTED;
+    } else {
+        switch (op) {
+        case AK_OP_ADD: return f(Tag<OpAdd>{});
+        case AK_OP_MUL: return f(Tag<OpMul>{});
+        case AK_OP_MAX: return f(Tag<OpMax>{});
+        case AK_OP_MIN: return f(Tag<OpMin>{});
+        default: return AK_ERR_UNSUPPORTED;
+        }
+    }
+}
+
+template <class Acc, class F>
+ak_status dispatch_map(ak_map m, F&& f) {
+    if constexpr (is_mat2_v<Acc>) {
+        if (m == AK_MAP_IDENTITY) return f(Tag<MapIdentity>{});
+        return AK_ERR_UNSUPPORTED;
+    } else {
+        switch (m) {
+        case AK_MAP_IDENTITY: return f(Tag<MapIdentity>{});
+        case AK_MAP_ABS: return f(Tag<MapAbs>{});
+        case AK_MAP_ABS2: return f(Tag<MapAbs2>{});
+        default: return AK_ERR_UNSUPPORTED;
+        }
+    }
+}
+
+template <class Op, class Acc, class F>
+ak_status dispatch_monoid(bool no_neutral, F&& f) {
+    if (no_neutral) return f(Tag<Lifted<Op, Acc>>{});
+    return f(Tag<Plain<Op, Acc>>{});
+}
+
+// Size of a partial result (accumulator, or Optional accumulator).
+size_t partial_size(ak_dtype acc, bool no_neutral);
+
+// ---------------------------------------------------------------------------
+// call descriptors (validated by api.cu)
+// ---------------------------------------------------------------------------
+struct alignas(16) Value16 {
+    unsigned char b[16];
+};
+
+struct ReduceCall {
+    const void* src;
+    int64_t n;  // > 0
+    ak_dtype in, acc, out;
+    ak_map f;
+    ak_op op;
+    bool no_neutral;
+    ak_store mode;
+    Value16 init;  // accumulator value (valid when mode == AK_STORE_INIT)
+    void* dst;     // device output element, or NULL when `bare` is used
+    void* bare;    // device slot for the bare partial result (host finish), or NULL
+    void* ws;
+    size_t ws_bytes;
+    int target_blocks;
+    cudaStream_t stream;
+};
+
+// Grid of the whole-array first pass and the workspace it needs.
+struct ReducePlan {
+    int grid;         // 1 = single launch
+    size_t ws_bytes;  // header + partials + bare slot
+    size_t partials_off, bare_off;
+};
+ak_status plan_reduce(int64_t n, ak_dtype in, ak_dtype acc, bool no_neutral, int target_blocks,
+                      const DeviceInfo& dev, ReducePlan* plan);
+ak_status run_reduce(const ReduceCall& c, const ReducePlan& plan);
+
+// Canonical strided problem: out[i + inner*k] = fold_j x[i + inner*(j + red*k)].
+struct DimsCall {
+    const void* src;
+    int64_t inner, red, outer;
+    ak_dtype in, acc, out;
+    ak_map f;
+    ak_op op;
+    bool no_neutral;
+    ak_store mode;
+    Value16 init;
+    void* dst;
+    void* ws;
+    size_t ws_bytes;
+    int forced_shape;
+    cudaStream_t stream;
+    // general fallback (any dims mask): full shape and mask
+    int ndim;
+    int64_t shape[8];
+    uint32_t mask;
+    bool general;
+};
+
+struct DimsPlan {
+    int shape;        // ak_dims_shape actually used
+    int vec;          // elements per vector load along the contiguous dimension
+    int tile_out;     // outputs per block along the contiguous dimension
+    int row_groups;   // reduction rows processed in parallel per block
+    int split;        // blocks along the reduction (> 1: second pass)
+    size_t ws_bytes;
+};
+ak_status plan_dims(const DimsCall& c, const DeviceInfo& dev, DimsPlan* plan);
+ak_status run_reduce_dims(const DimsCall& c, const DimsPlan& plan);
+// Fills R where the reduction is empty (store rules of ak_reduce).
+ak_status run_fill(void* dst, int64_t count, ak_dtype out, const Value16& value, cudaStream_t s);
+
+struct ScanCall {
+    const void* src;
+    void* dst;
+    int64_t inner, len, outer;  // line of `len` elements at stride `inner`; inner*outer lines
+    ak_dtype in, acc, out;
+    ak_op op;
+    bool no_neutral;
+    bool has_init;
+    Value16 init;
+    void* ws;
+    size_t ws_bytes;
+    int target_blocks;
+    int items;
+    int64_t wait_limit_ns;
+    int64_t skip_tile;
+    uint64_t epoch;
+    cudaStream_t stream;
+};
+struct ScanPlan {
+    int kind;        // 0 = tile scan of contiguous lines, 1 = strided (inner > 1)
+    int block, items;
+    int grid;
+    int64_t tiles_per_line, tiles;
+    size_t state_off, ws_bytes;
+};
+ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_dtype acc,
+                    ak_op op, bool no_neutral, int target_blocks, int items,
+                    const DeviceInfo& dev, ScanPlan* plan);
+ak_status run_scan(const ScanCall& c, const ScanPlan& plan);
+
+}  // namespace ak

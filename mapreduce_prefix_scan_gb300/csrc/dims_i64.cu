@@ -1,0 +1,7 @@
+// dims_i64.cu -- strided / contiguous / general dims-reduction kernels for
+// i64 input (one translation unit per input type, built in parallel).
+#include "reduce_dims.cuh"
+
+namespace ak {
+ak_status run_dims_i64(const DimsCall& c, const DimsPlan& p) { return dims::run_for_input<int64_t>(c, p); }
+}  // namespace ak

@@ -1,0 +1,138 @@
+// reduce_dims.cu -- host side of the reductions over a set of dimensions:
+// shape selection, workspace plan, dispatch by input type to the kernel
+// translation units (dims_*.cu), and the fill used for empty reductions.
+// The kernels and their design notes are in reduce_dims.cuh.
+#include <algorithm>
+
+#include "reduce_dims.cuh"
+
+namespace ak {
+
+ak_status run_dims_f32(const DimsCall& c, const DimsPlan& p);
+ak_status run_dims_bf16(const DimsCall& c, const DimsPlan& p);
+ak_status run_dims_f64(const DimsCall& c, const DimsPlan& p);
+ak_status run_dims_i32(const DimsCall& c, const DimsPlan& p);
+ak_status run_dims_i64(const DimsCall& c, const DimsPlan& p);
+ak_status run_dims_mat2(const DimsCall& c, const DimsPlan& p);
+
+namespace {
+
+using dims::kBlock;
+using dims::kMinRowsPerGroup;
+
+template <class Out>
+__global__ void k_fill(Out* dst, int64_t count, Out v) {
+    const int64_t i = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    if (i < count) dst[i] = v;
+}
+
+}  // namespace
+
+// Shape selection for the strided form (see k_dims_strided). The block has
+// kBlock threads; a row segment of tile_out outputs is read by tpr <= 32
+// threads with vec-wide loads. The reduction is split only as far as needed
+// to give the device about target_ctas blocks, and never below
+// kMinRowsPerGroup rows per group.
+static void select_shape(int64_t I, int64_t J, int64_t K, int vec, int sm_count, int forced,
+                         DimsPlan* p) {
+    const int64_t target_ctas = (int64_t)sm_count * (2048 / kBlock);
+    const int64_t vecs_per_row = (I + vec - 1) / vec;
+    // Enough outputs that one thread per vector of outputs already puts
+    // kUnroll loads in flight on every thread slot of the device.
+    const bool many_outputs = vecs_per_row * K >= (int64_t)sm_count * 2048;
+    int shape = forced;
+    if (shape == AK_SHAPE_AUTO) shape = (J < 32 || many_outputs) ? AK_SHAPE_THREAD : AK_SHAPE_COLUMNS;
+    p->vec = vec;
+    if (shape == AK_SHAPE_THREAD) {
+        const int tpr = (int)std::min<int64_t>(kBlock, vecs_per_row);
+        p->tile_out = tpr * vec;
+        p->row_groups = 1;
+        p->split = 1;
+        p->shape = AK_SHAPE_THREAD;
+        return;
+    }
+    const int tpr = (int)std::min<int64_t>(32, vecs_per_row);
+    p->tile_out = tpr * vec;
+    p->row_groups = kBlock / tpr;
+    const int64_t col_tiles = ((I + p->tile_out - 1) / p->tile_out) * K;
+    int64_t split = (target_ctas + col_tiles - 1) / col_tiles;
+    const int64_t max_split = std::max<int64_t>(1, J / ((int64_t)p->row_groups * kMinRowsPerGroup));
+    split = std::max<int64_t>(1, std::min<int64_t>(split, max_split));
+    split = std::min<int64_t>(split, 65535);
+    if (shape == AK_SHAPE_TILED) split = 1;
+    if (shape == AK_SHAPE_COLUMNS && forced == AK_SHAPE_COLUMNS && split == 1 && J >= 2) split = 2;
+    p->split = (int)split;
+    p->shape = split > 1 ? AK_SHAPE_COLUMNS : AK_SHAPE_TILED;
+}
+
+ak_status plan_dims(const DimsCall& c, const DeviceInfo& dev, DimsPlan* p) {
+    const size_t psz = partial_size(c.acc, c.no_neutral);
+    const size_t esz = ak_dtype_size(c.in);
+    if (!psz || !esz) return AK_ERR_UNSUPPORTED;
+    p->ws_bytes = kWsHeader;
+    p->split = 1;
+    p->vec = 1;
+    p->tile_out = 1;
+    p->row_groups = 1;
+    p->shape = AK_SHAPE_THREAD;
+    if (c.general) return AK_OK;
+    if (c.inner == 1) {
+        // contiguous reduction: split long rows when there are few outputs
+        const int64_t target_warps = (int64_t)dev.sm_count * 64;
+        int64_t split = (target_warps + c.outer - 1) / c.outer;
+        split = std::max<int64_t>(1, std::min<int64_t>(split, c.red / 1024));
+        p->split = (int)split;
+        p->shape = split > 1 ? AK_SHAPE_COLUMNS : AK_SHAPE_TILED;
+    } else {
+        const uintptr_t addr = reinterpret_cast<uintptr_t>(c.src);
+        int vec = 1;
+        if (esz < 16 && addr % 16 == 0 && (c.inner * (int64_t)esz) % 16 == 0) vec = (int)(16 / esz);
+        select_shape(c.inner, c.red, c.outer, vec, dev.sm_count, c.forced_shape, p);
+    }
+    if (p->split > 1) p->ws_bytes = align_up(kWsHeader + (size_t)p->split * c.inner * c.outer * psz, 256);
+    return AK_OK;
+}
+
+ak_status run_reduce_dims(const DimsCall& c, const DimsPlan& plan) {
+    switch (c.in) {
+    case AK_F32: return run_dims_f32(c, plan);
+    case AK_BF16: return run_dims_bf16(c, plan);
+    case AK_F64: return run_dims_f64(c, plan);
+    case AK_I32: return run_dims_i32(c, plan);
+    case AK_I64: return run_dims_i64(c, plan);
+    case AK_MAT2_MODP: return run_dims_mat2(c, plan);
+    default: return AK_ERR_UNSUPPORTED;
+    }
+}
+
+ak_status run_fill(void* dst, int64_t count, ak_dtype out, const Value16& value, cudaStream_t s) {
+    if (count <= 0) return AK_OK;
+    const unsigned blocks = (unsigned)((count + kBlock - 1) / kBlock);
+    switch (ak_dtype_size(out)) {
+    case 2: { uint16_t v; memcpy(&v, value.b, 2); k_fill<uint16_t><<<blocks, kBlock, 0, s>>>((uint16_t*)dst, count, v); break; }
+    case 4: { uint32_t v; memcpy(&v, value.b, 4); k_fill<uint32_t><<<blocks, kBlock, 0, s>>>((uint32_t*)dst, count, v); break; }
+    case 8: { uint64_t v; memcpy(&v, value.b, 8); k_fill<uint64_t><<<blocks, kBlock, 0, s>>>((uint64_t*)dst, count, v); break; }
+    case 16: { Mat2 v; memcpy(&v, value.b, 16); k_fill<Mat2><<<blocks, kBlock, 0, s>>>((Mat2*)dst, count, v); break; }
+    default: return AK_ERR_UNSUPPORTED;
+    }
+    ak_status st = check_launch();
+    if (st == AK_OK) count_launches(1);
+    return st;
+}
+
+}  // namespace ak
+
+extern "C" ak_status ak_dims_select(int64_t inner, int64_t red_len, int64_t outer, int elem_bytes,
+                                    int vec_elems, int sm_count, int forced_shape, int32_t* shape_out,
+                                    int32_t* tile_outputs, int32_t* row_groups, int32_t* split) {
+    if (inner < 1 || red_len < 1 || outer < 1 || elem_bytes < 1 || vec_elems < 1 || sm_count < 1 ||
+        forced_shape < AK_SHAPE_AUTO || forced_shape > AK_SHAPE_COLUMNS || vec_elems * elem_bytes > 16)
+        return AK_ERR_INVALID_ARG;
+    ak::DimsPlan p = {};
+    ak::select_shape(inner, red_len, outer, vec_elems, sm_count, forced_shape, &p);
+    if (shape_out) *shape_out = p.shape;
+    if (tile_outputs) *tile_outputs = p.tile_out;
+    if (row_groups) *row_groups = p.row_groups;
+    if (split) *split = p.split;
+    return AK_OK;
+}

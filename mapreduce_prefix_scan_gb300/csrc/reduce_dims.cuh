@@ -1,0 +1,339 @@
+// reduce_dims.cuh -- kernels of the reductions over a set of dimensions of a dense
+// column-major array on GB300.
+//
+// After merging dimensions (api.cu), most problems take one of two canonical
+// forms:
+//   strided  out[i + I*k] = fold_j x[i + I*(j + J*k)]   (I > 1: outputs are
+//            contiguous, the reduction walks rows at stride I: sum(x; dims=2)
+//            of a matrix, the middle dimension of a 3-d array)
+//   rows     out[k]       = fold_j x[j + J*k]           (contiguous reduction)
+// anything else goes to a general one-thread-per-output kernel.
+//
+// Strided kernel (strided-reduction PR #176, item 1 and the paragraph after
+// it: a fixed 2-d block of outputs x reduction rows, split across blocks only
+// when the outputs alone do not fill the device; item 2: runs of contiguous
+// outputs at the offsets of the other kept dimensions, so the middle
+// dimension of a 3-d array takes the same kernel). A block owns a tile of
+// `tile_out` consecutive outputs of one run k and a range of reduction rows.
+// Its threads form `row_groups` groups of `tpr` threads; a group covers the
+// tile's row segment with 16-byte vector loads and walks a contiguous
+// sub-range of rows with several rows in flight. Groups are combined in row
+// order through shared memory, so non-commutative operators keep their
+// order. With a split, per-split partials go to the workspace and a second
+// pass (programmatic dependent launch) folds them in split order.
+//
+// The three shapes of the pages are parameter regimes of this one kernel:
+// "thread" = one group (each thread owns vec outputs and walks all rows),
+// "tiled" = several groups, no split, "columns" = several groups and a split.
+#pragma once
+#include <algorithm>
+
+#include "ak_common.cuh"
+#include "ak_internal.h"
+
+namespace ak {
+namespace dims {
+
+constexpr int kBlock = 256;
+constexpr int kUnroll = 4;          // rows in flight per thread
+constexpr int kMinRowsPerGroup = 8; // the selector splits no further than this many rows per group
+
+template <class Acc, class Out, class M>
+struct DimsStore {
+    int mode;
+    Acc init;
+    Out* dst;
+};
+
+template <class Acc, class Out, class M>
+__device__ __forceinline__ void dims_store(const typename M::P& r, const DimsStore<Acc, Out, M>& st,
+                                           int64_t o) {
+    using Op = typename M::op;
+    Acc v = M::value(r);
+    if (st.mode == AK_STORE_INIT) v = Op::apply(st.init, v);
+    else if (st.mode == AK_STORE_FOLD) v = Op::apply(convert<Acc>(st.dst[o]), v);
+    st.dst[o] = convert<Out>(v);
+}
+
+template <class In, class Acc, class Map, class M>
+__device__ __forceinline__ typename M::P lift_elem(In x) {
+    return M::lift(Map::apply(convert<Acc>(x)));
+}
+
+// One row segment of VB bytes: a 16-byte streaming vector load, or a single
+// element.
+template <class In, int VB>
+__device__ __forceinline__ void load_row(const In* p, In (&r)[VB / sizeof(In)]) {
+    if constexpr (VB == 16 && sizeof(In) < 16) {
+        Raw<16> t = ld_stream16(p);
+        memcpy(r, &t, 16);
+    } else {
+        r[0] = *p;
+    }
+}
+
+// VB = bytes per load: 16 (vector of 16/sizeof(In) outputs) or sizeof(In).
+template <class In, class Acc, class Out, class Map, class M, int VB>
+__global__ void __launch_bounds__(kBlock) k_dims_strided(const In* __restrict__ x, int64_t I, int64_t J,
+                                                         int64_t K, int tile_out, int tpr, int R,
+                                                         int split, typename M::P* __restrict__ partials,
+                                                         DimsStore<Acc, Out, M> st) {
+    using P = typename M::P;
+    constexpr int V = VB / (int)sizeof(In);
+    __shared__ P smem[kBlock * V];
+
+    const int64_t tiles_i = (I + tile_out - 1) / tile_out;
+    const int64_t ct = blockIdx.x % tiles_i, k = blockIdx.x / tiles_i;
+    const int s = blockIdx.y;
+    const int tid = threadIdx.x, c = tid % tpr, rg = tid / tpr;
+    const int64_t i0 = ct * tile_out + (int64_t)c * V;
+
+    const int64_t jper = (J + split - 1) / split;
+    const int64_t js = (int64_t)s * jper, je = min(J, js + jper);
+    const int64_t rper = (je - js + R - 1) / R;
+    const int64_t jr = min(je, js + rg * rper), jre = min(je, jr + rper);
+
+    P acc[V];
+#pragma unroll
+    for (int q = 0; q < V; ++q) acc[q] = M::empty();
+
+    if (rg < R && i0 < I) {
+        const In* base = x + i0 + I * J * k;
+        if (i0 + V <= I) {
+            int64_t j = jr;
+            for (; j + kUnroll <= jre; j += kUnroll) {
+                In r[kUnroll][V];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) load_row<In, VB>(base + I * (j + u), r[u]);
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+                    for (int q = 0; q < V; ++q)
+                        acc[q] = M::combine(acc[q], lift_elem<In, Acc, Map, M>(r[u][q]));
+            }
+            for (; j < jre; ++j) {
+                In r[V];
+                load_row<In, VB>(base + I * j, r);
+#pragma unroll
+                for (int q = 0; q < V; ++q) acc[q] = M::combine(acc[q], lift_elem<In, Acc, Map, M>(r[q]));
+            }
+        } else {
+            // ragged last vector of the row: scalar loads of the valid columns
+            for (int64_t j = jr; j < jre; ++j)
+#pragma unroll
+                for (int q = 0; q < V; ++q)
+                    if (i0 + q < I) acc[q] = M::combine(acc[q], lift_elem<In, Acc, Map, M>(base[I * j + q]));
+        }
+    }
+    griddep_launch_dependents();
+
+    // smem[rg][c*V + q]; group rows are contiguous ranges, combined in order
+    if (rg < R) {
+#pragma unroll
+        for (int q = 0; q < V; ++q) smem[rg * tile_out + c * V + q] = acc[q];
+    }
+    __syncthreads();
+    for (int o = tid; o < tile_out; o += kBlock) {
+        const int64_t i = ct * tile_out + o;
+        if (i >= I) continue;
+        P a = smem[o];
+        for (int g = 1; g < R; ++g) a = M::combine(a, smem[g * tile_out + o]);
+        if (split == 1) dims_store<Acc, Out, M>(a, st, i + I * k);
+        else partials[((int64_t)s * K + k) * I + i] = a;
+    }
+}
+
+// Contiguous reduction: one warp per (output k, split s) segment.
+template <class In, class Acc, class Out, class Map, class M>
+__global__ void __launch_bounds__(kBlock) k_dims_rows(const In* __restrict__ x, int64_t J, int64_t K,
+                                                      int split, typename M::P* __restrict__ partials,
+                                                      DimsStore<Acc, Out, M> st) {
+    using P = typename M::P;
+    constexpr int kRun = 8;
+    const int lane = threadIdx.x % kWarp;
+    const int64_t gw = (int64_t)blockIdx.x * (kBlock / kWarp) + threadIdx.x / kWarp;
+    if (gw >= K * split) return;
+    const int64_t k = gw / split;
+    const int s = (int)(gw % split);
+    const int64_t jper = (J + split - 1) / split;
+    const int64_t js = (int64_t)s * jper, je = min(J, js + jper);
+    const In* row = x + J * k;
+    P a = M::empty();
+    if constexpr (M::commutative) {
+        int64_t j = js + lane;
+        for (; j + 3 * kWarp < je; j += 4 * kWarp) {
+            In v0 = row[j], v1 = row[j + kWarp], v2 = row[j + 2 * kWarp], v3 = row[j + 3 * kWarp];
+            a = M::combine(a, lift_elem<In, Acc, Map, M>(v0));
+            a = M::combine(a, lift_elem<In, Acc, Map, M>(v1));
+            a = M::combine(a, lift_elem<In, Acc, Map, M>(v2));
+            a = M::combine(a, lift_elem<In, Acc, Map, M>(v3));
+        }
+        for (; j < je; j += kWarp) a = M::combine(a, lift_elem<In, Acc, Map, M>(row[j]));
+        a = warp_reduce<M>(a);
+    } else {
+        for (int64_t c = js; c < je; c += kWarp * kRun) {
+            P r = M::empty();
+            const int64_t b = c + (int64_t)lane * kRun;
+#pragma unroll
+            for (int q = 0; q < kRun; ++q)
+                if (b + q < je) r = M::combine(r, lift_elem<In, Acc, Map, M>(row[b + q]));
+            r = warp_reduce<M>(r);
+            a = M::combine(a, r);
+        }
+    }
+    griddep_launch_dependents();
+    if (lane == 0) {
+        if (split == 1) dims_store<Acc, Out, M>(a, st, k);
+        else partials[(int64_t)s * K + k] = a;
+    }
+}
+
+// Second pass of a split: output o folds partials[s*nout + o], s = 0..split-1.
+template <class Acc, class Out, class M>
+__global__ void __launch_bounds__(kBlock) k_dims_finish(const typename M::P* partials, int64_t nout,
+                                                        int split, DimsStore<Acc, Out, M> st) {
+    griddep_wait();
+    const int64_t o = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    if (o >= nout) return;
+    typename M::P a = partials[o];
+    for (int s = 1; s < split; ++s) a = M::combine(a, partials[(int64_t)s * nout + o]);
+    dims_store<Acc, Out, M>(a, st, o);
+}
+
+// General fallback for any dims mask: one thread per output, reduced indices
+// visited in increasing column-major order.
+struct GeneralIndex {
+    int ndim;
+    int64_t shape[8];
+    int64_t stride[8];
+    int nk, nr;
+    int kept[8], red[8];
+    int64_t nout, nfold;
+};
+
+template <class In, class Acc, class Out, class Map, class M>
+__global__ void __launch_bounds__(kBlock) k_dims_general(const In* __restrict__ x, GeneralIndex g,
+                                                         DimsStore<Acc, Out, M> st) {
+    const int64_t o = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    if (o >= g.nout) return;
+    int64_t base = 0, t = o;
+    for (int a = 0; a < g.nk; ++a) {
+        const int d = g.kept[a];
+        base += (t % g.shape[d]) * g.stride[d];
+        t /= g.shape[d];
+    }
+    typename M::P acc = M::empty();
+    for (int64_t r = 0; r < g.nfold; ++r) {
+        int64_t off = base, u = r;
+        for (int a = 0; a < g.nr; ++a) {
+            const int d = g.red[a];
+            off += (u % g.shape[d]) * g.stride[d];
+            u /= g.shape[d];
+        }
+        acc = M::combine(acc, lift_elem<In, Acc, Map, M>(x[off]));
+    }
+    dims_store<Acc, Out, M>(acc, st, o);
+}
+
+template <class Acc, class Out, class M, class... Args>
+cudaError_t launch_finish(dim3 grid, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kBlock);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_dims_finish<Acc, Out, M>, args...);
+}
+
+template <class In, class Acc, class Out, class Map, class M>
+ak_status launch(const DimsCall& c, const DimsPlan& p) {
+    using P = typename M::P;
+    DimsStore<Acc, Out, M> st;
+    st.mode = c.mode;
+    memcpy(&st.init, c.init.b, sizeof(Acc));
+    st.dst = static_cast<Out*>(c.dst);
+    P* partials = reinterpret_cast<P*>(static_cast<char*>(c.ws) + kWsHeader);
+    const In* x = static_cast<const In*>(c.src);
+    if (c.general) {
+        GeneralIndex g = {};
+        g.ndim = c.ndim;
+        int64_t stv = 1;
+        g.nout = g.nfold = 1;
+        for (int d = 0; d < c.ndim; ++d) {
+            g.shape[d] = c.shape[d];
+            g.stride[d] = stv;
+            stv *= c.shape[d];
+            if ((c.mask >> d) & 1u) { g.red[g.nr++] = d; g.nfold *= c.shape[d]; }
+            else { g.kept[g.nk++] = d; g.nout *= c.shape[d]; }
+        }
+        const int64_t blocks = (g.nout + kBlock - 1) / kBlock;
+        k_dims_general<In, Acc, Out, Map, M><<<(unsigned)blocks, kBlock, 0, c.stream>>>(x, g, st);
+        ak_status s = check_launch();
+        if (s == AK_OK) count_launches(1);
+        return s;
+    }
+    const int64_t nout = c.inner * c.outer;
+    if (c.inner == 1) {
+        const int64_t warps = c.outer * p.split;
+        const int64_t blocks = (warps + kBlock / kWarp - 1) / (kBlock / kWarp);
+        k_dims_rows<In, Acc, Out, Map, M><<<(unsigned)blocks, kBlock, 0, c.stream>>>(x, c.red, c.outer, p.split,
+                                                                                    partials, st);
+    } else {
+        const int64_t tiles_i = (c.inner + p.tile_out - 1) / p.tile_out;
+        const int tpr = p.tile_out / p.vec;
+        dim3 grid((unsigned)(tiles_i * c.outer), (unsigned)p.split);
+        if (p.vec > 1) {
+            if constexpr (16 % sizeof(In) == 0 && sizeof(In) < 16)
+                k_dims_strided<In, Acc, Out, Map, M, 16><<<grid, kBlock, 0, c.stream>>>(
+                    x, c.inner, c.red, c.outer, p.tile_out, tpr, p.row_groups, p.split, partials, st);
+        } else {
+            k_dims_strided<In, Acc, Out, Map, M, (int)sizeof(In)><<<grid, kBlock, 0, c.stream>>>(
+                x, c.inner, c.red, c.outer, p.tile_out, tpr, p.row_groups, p.split, partials, st);
+        }
+    }
+    ak_status s = check_launch();
+    if (s != AK_OK) return s;
+    count_launches(1);
+    if (p.split > 1) {
+        dim3 grid((unsigned)((nout + kBlock - 1) / kBlock));
+        cudaError_t e = launch_finish<Acc, Out, M>(grid, c.stream, (const P*)partials, nout, p.split, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        count_launches(1);
+    }
+    return AK_OK;
+}
+
+// Runs the reduction for one input type: dispatches the accumulator /
+// output types, operator, map and monoid. Each dims_*.cu instantiates it for
+// its input types, so the kernels compile in parallel translation units.
+template <class In>
+ak_status run_for_input(const DimsCall& c, const DimsPlan& plan) {
+    return dispatch_types(c.in, c.acc, c.out, [&](auto ti, auto ta, auto to) -> ak_status {
+        using In2 = typename decltype(ti)::type;
+        using Acc = typename decltype(ta)::type;
+        using Out = typename decltype(to)::type;
+        if constexpr (!std::is_same_v<In, In2>) {
+            return AK_ERR_UNSUPPORTED;
+        } else {
+            return dispatch_op<Acc>(c.op, [&](auto top) -> ak_status {
+                using Op = typename decltype(top)::type;
+                if (c.no_neutral) {
+                    // Optional partials: identity map only
+                    if (c.f != AK_MAP_IDENTITY) return AK_ERR_UNSUPPORTED;
+                    return launch<In, Acc, Out, MapIdentity, Lifted<Op, Acc>>(c, plan);
+                }
+                return dispatch_map<Acc>(c.f, [&](auto tm) -> ak_status {
+                    using Map = typename decltype(tm)::type;
+                    return launch<In, Acc, Out, Map, Plain<Op, Acc>>(c, plan);
+                });
+            });
+        }
+    });
+}
+
+}  // namespace dims
+}  // namespace ak

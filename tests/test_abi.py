@@ -1,0 +1,125 @@
+"""CPU checks of the C ABI: the library loads, exports every symbol that
+include/ak.h declares, and validates arguments before touching a device.
+The dims shape selector and the scan workspace plan are pure host logic."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mapreduce_prefix_scan_gb300 import build
+    build.build()
+    from mapreduce_prefix_scan_gb300 import _abi
+    return _abi.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "ak.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ak_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    from mapreduce_prefix_scan_gb300 import _abi
+    names = _declared()
+    assert set(names) == set(_abi.EXPORTS)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_sizes(L):
+    for s in range(7):
+        assert L.ak_status_string(s)
+    assert L.ak_status_string(99) == b"unknown status"
+    assert [L.ak_dtype_size(t) for t in range(6)] == [4, 8, 2, 4, 8, 16]
+    assert L.ak_dtype_size(17) == 0
+
+
+def test_opts_default(L):
+    from mapreduce_prefix_scan_gb300 import _abi
+    o = _abi.ak_opts()
+    o.no_neutral = 7
+    L.ak_opts_default(ctypes.byref(o))
+    assert o.no_neutral == 0 and o.dims_shape == 0 and o.debug_skip_publish_tile == -1
+    assert ctypes.sizeof(_abi.ak_opts) == 40
+
+
+def _reduce(L, src=0x1000, n=10, in_t=0, f=0, op=0, acc=0, out=0, init=None, mode=0, dst=0x2000, host=None):
+    return L.ak_reduce(src, n, in_t, f, op, acc, out, init, mode, dst, host, 0x4000, 1 << 20, None, None)
+
+
+def test_reduce_validates_before_device(L):
+    from mapreduce_prefix_scan_gb300._abi import AK_ERR_INVALID_ARG as INV, AK_ERR_UNSUPPORTED as UNS
+    assert _reduce(L, in_t=9) == INV
+    assert _reduce(L, f=5) == INV
+    assert _reduce(L, op=8) == INV
+    assert _reduce(L, n=-1) == INV
+    assert _reduce(L, src=None) == INV
+    assert _reduce(L, dst=None, host=None) == INV
+    assert _reduce(L, mode=3) == INV
+    assert _reduce(L, mode=1, init=None) == INV            # init mode without init
+    assert _reduce(L, src=0x1001) == INV                   # misaligned f32 source
+    assert _reduce(L, in_t=5, acc=5, out=5, op=0) == UNS    # matrices only multiply
+    assert _reduce(L, in_t=0, acc=0, out=0, op=4) == UNS    # matmul needs matrices
+    assert _reduce(L, in_t=5, acc=5, out=5, op=4, f=2) == UNS
+    assert _reduce(L, in_t=2, acc=2, out=2) == UNS          # bf16 accumulator
+    assert _reduce(L, in_t=4, acc=3, out=3) == UNS          # narrowing accumulator
+
+
+def test_reduce_dims_validates_before_device(L):
+    from mapreduce_prefix_scan_gb300._abi import AK_ERR_INVALID_ARG as INV
+    sh = (ctypes.c_int64 * 3)(4, 5, 6)
+    call = lambda ndim=3, shape=sh, mask=2, mode=0, init=None: L.ak_reduce_dims(
+        0x1000, ndim, shape, mask, 0, 0, 0, 0, 0, init, mode, 0x2000, 0x4000, 1 << 20, None, None)
+    assert call(ndim=0) == INV
+    assert call(ndim=9) == INV
+    assert call(mask=1 << 3) == INV
+    assert call(shape=None) == INV
+    assert call(shape=(ctypes.c_int64 * 3)(4, -1, 6)) == INV
+    assert call(mode=1) == INV
+
+
+def test_accumulate_validates_and_plans_on_host(L):
+    from mapreduce_prefix_scan_gb300._abi import AK_ERR_INVALID_ARG as INV, AK_ERR_UNSUPPORTED as UNS
+    sh = (ctypes.c_int64 * 2)(4096, 4096)
+    acc = lambda dim=0, src=0x1000, dst=0x800000, in_t=0, op=0, a=0, o=0: L.ak_accumulate(
+        src, dst, 2, sh, dim, in_t, op, a, o, None, 0x4000, 1 << 20, None, None)
+    assert acc(dim=2) == INV
+    assert acc(dim=-2) == INV
+    assert acc(src=None) == INV
+    assert acc(dst=0x1000 + 64) == INV        # partial overlap
+    assert acc(in_t=5, a=5, o=5, op=0) == UNS
+    b = ctypes.c_size_t()
+    # whole-array f64 scan of 1e8: 512 x 8 tiles, one state word + two partials each
+    n = (ctypes.c_int64 * 1)(10**8)
+    assert L.ak_accumulate_workspace_size(1, n, -1, 1, 1, 0, None, ctypes.byref(b)) == 0
+    tiles = -(-10**8 // 4096)
+    assert b.value >= 256 + tiles * (8 + 16)
+    # columns of 4096 f32 fit one tile each: no tile state needed
+    assert L.ak_accumulate_workspace_size(2, sh, 0, 0, 0, 0, None, ctypes.byref(b)) == 0
+    assert b.value == 256
+
+
+def test_dims_selector(L):
+    import mapreduce_prefix_scan_gb300 as ak
+    # 3072 x 2048 bf16, dims=2: 16-byte vectors of 8, tiles of 256 outputs, split
+    shape, tile, groups, split = ak.ak_dims_select(3072, 2048, 1, 2, 8, 152)
+    assert shape == "columns" and tile == 256 and groups == 8 and split > 1
+    assert -(-3072 // tile) * split >= 152
+    # middle dim of 64 x 4096 x 32 f32: 64-output tiles, one run per k
+    shape, tile, groups, split = ak.ak_dims_select(64, 4096, 32, 4, 4, 152)
+    assert tile == 64 and groups == 16 and shape == "columns"
+    # short reductions take one thread per output vector
+    assert ak.ak_dims_select(100_000, 16, 1, 4, 4, 152)[0] == "thread"
+    # forced shapes are honoured
+    assert ak.ak_dims_select(3072, 2048, 1, 2, 8, 152, "tiled")[3] == 1
+    assert ak.ak_dims_select(3072, 2048, 1, 2, 8, 152, "thread")[2] == 1
+    with pytest.raises(ak.AkError):
+        ak.ak_dims_select(0, 1, 1, 4, 4, 152)

@@ -1,0 +1,178 @@
+"""GPU parity of ak_accumulate (inclusive scans) against the oracle.
+
+The scan workloads at full size: cumsum of 1e8 f64; accumulate! of 1e7 f32
+with max under Optional partials (no neutral element); cumsum along
+dims=1 (Julia) of a 4096x4096 f32 matrix; the prefix product of 1e7 2x2
+matrices mod 2^31-1, whole and along dims=1 of 1024x8192 matrices
+(tile-scan PR #202: runs of each parity and partials of 4 to 16 bytes, whole
+and along dims). Plus ragged sizes, init, in-place, strided dims, and the
+bounded look-back wait running out on an injected missing publication.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import mapreduce_prefix_scan_gb300 as ak
+import oracle
+import synth
+from helpers import F64_REL, assert_close_f32, assert_exact, dev_of, gen
+
+pytestmark = pytest.mark.gpu
+
+
+def _mass_lines(x64, shape, dim):
+    a = np.abs(x64)
+    if dim < 0:
+        return np.cumsum(a)
+    return np.cumsum(a.reshape(tuple(reversed(shape))), axis=len(shape) - 1 - dim).ravel()
+
+
+# --------------------------------------------------------------------------
+# the scan workloads at full size
+# --------------------------------------------------------------------------
+
+def test_cumsum_1e8_f64():
+    x = synth.uniform_f64_01(10**8, seed=0, stream=60)
+    y = ak.ak_accumulate(dev_of("f64", x)).cpu().numpy()
+    want = oracle.scan(x, "f64")
+    assert_close_f32(y, want, np.cumsum(x), rel=F64_REL)
+
+
+def test_accumulate_max_1e7_f32_no_neutral():
+    x = synth.normal_f32(10**7, seed=0, stream=61)
+    y = ak.ak_accumulate(dev_of("f32", x), op="max", opts=ak.make_opts(no_neutral=True)).cpu().numpy()
+    assert_exact(y.astype(np.float64), oracle.scan(x, "f32", op="max"))
+
+
+def test_cumsum_dims1_4096x4096_f32():
+    shape = (4096, 4096)
+    x = synth.normal_f32(4096 * 4096, seed=0, stream=62)
+    y = ak.ak_accumulate(dev_of("f32", x).reshape(4096, 4096), dim=0).cpu().numpy()
+    want = oracle.scan(x, "f32", shape, 0)
+    assert_close_f32(y, want, _mass_lines(x.astype(np.float64), shape, 0))
+
+
+def test_mat2_prefix_product_1e7():
+    x = synth.mat2_modp(10**7, seed=0, stream=63)
+    y = ak.ak_accumulate(dev_of("mat2", x), op="matmul", elem="mat2").cpu().numpy().view(np.uint32)
+    assert_exact(y.reshape(-1, 4), oracle.scan(x, "mat2"))
+
+
+def test_mat2_prefix_product_dims1_1024x8192():
+    shape = (1024, 8192)
+    x = synth.mat2_modp(1024 * 8192, seed=0, stream=64)
+    xd = dev_of("mat2", x).reshape(8192, 1024, 4)
+    y = ak.ak_accumulate(xd, op="matmul", elem="mat2", dim=0).cpu().numpy().view(np.uint32)
+    assert_exact(y.reshape(-1, 4), oracle.scan(x, "mat2", shape, 0))
+
+
+# --------------------------------------------------------------------------
+# sizes, types, operators, init, in place
+# --------------------------------------------------------------------------
+
+SIZES = [1, 2, 31, 127, 128, 1023, 1024, 2047, 4096, 4097, 8191, 8192, 8193, 3 * 8192 + 5, 100_003, 1_234_567]
+
+
+@pytest.mark.parametrize("n", SIZES)
+def test_sizes_f32_f64_i64(n):
+    x = gen("f32", n, stream=65, dist="normal")
+    y = ak.ak_accumulate(dev_of("f32", x)).cpu().numpy()
+    assert_close_f32(y, oracle.scan(x, "f32"), np.cumsum(np.abs(x.astype(np.float64))))
+    xd = gen("f64", n, stream=66, dist="normal")
+    y = ak.ak_accumulate(dev_of("f64", xd)).cpu().numpy()
+    assert_close_f32(y, oracle.scan(xd, "f64"), np.cumsum(np.abs(xd)), rel=F64_REL)
+    xi = gen("i64", n, stream=67)
+    assert_exact(ak.ak_accumulate(dev_of("i64", xi)).cpu().numpy(), oracle.scan(xi, "i64"))
+
+
+@pytest.mark.parametrize("n", [1, 100, 4096, 4097, 50_001])
+@pytest.mark.parametrize("kind,acc,out", [("i32", "i32", "i32"), ("i32", "i64", "i64"), ("f32", "f64", "f64"),
+                                          ("f32", "f64", "f32")])
+@pytest.mark.parametrize("op", ["add", "max", "min", "mul"])
+def test_types_ops(n, kind, acc, out, op):
+    x = gen(kind, n, stream=68)
+    if op == "mul":
+        x = (np.sign(x) + (x == 0)).astype(x.dtype)  # +-1: products stay exact
+    y = ak.ak_accumulate(dev_of(kind, x), op=op, acc=acc, out=out).cpu().numpy()
+    if kind == "i32":
+        assert_exact(y, oracle.scan(x, "i32", op=op, acc_bits=32 if acc == "i32" else 64))
+    else:
+        want = oracle.scan(x, "f32", op=op)
+        if out == "f32" and op == "add":
+            assert_close_f32(y, want, np.cumsum(np.abs(x.astype(np.float64))))
+        elif op == "add":
+            assert_close_f32(y, want, np.cumsum(np.abs(x.astype(np.float64))), rel=F64_REL)
+        else:
+            assert_exact(y.astype(np.float64), want)
+
+
+@pytest.mark.parametrize("no_neutral", [False, True])
+@pytest.mark.parametrize("op", ["add", "max", "min"])
+def test_init_and_optional(no_neutral, op):
+    n = 70_001
+    x = gen("i64", n, stream=69)
+    opts = ak.make_opts(no_neutral=no_neutral)
+    y = ak.ak_accumulate(dev_of("i64", x), op=op, init=12345, opts=opts).cpu().numpy()
+    assert_exact(y, oracle.scan(x, "i64", op=op, init=12345))
+    y = ak.ak_accumulate(dev_of("i64", x), op=op, opts=opts).cpu().numpy()
+    assert_exact(y, oracle.scan(x, "i64", op=op))
+
+
+def test_in_place():
+    x = gen("f64", 500_000, stream=70)
+    xd = dev_of("f64", x)
+    ak.ak_accumulate(xd, dst=xd)
+    assert_close_f32(xd.cpu().numpy(), oracle.scan(x, "f64"), np.cumsum(np.abs(x)), rel=F64_REL)
+
+
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 1023, 1024, 1025, 3000, 123_457])
+def test_mat2_sizes_and_init(n):
+    x = synth.mat2_modp(n, stream=71)
+    y = ak.ak_accumulate(dev_of("mat2", x), op="matmul", elem="mat2").cpu().numpy().view(np.uint32)
+    assert_exact(y.reshape(-1, 4), oracle.scan(x, "mat2"))
+    init = synth.mat2_modp(1, stream=72)[0]
+    y = ak.ak_accumulate(dev_of("mat2", x), op="matmul", elem="mat2", init=init,
+                         opts=ak.make_opts(no_neutral=True)).cpu().numpy().view(np.uint32)
+    assert_exact(y.reshape(-1, 4), oracle.scan(x, "mat2", init=init))
+
+
+# --------------------------------------------------------------------------
+# along dimensions
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape,dim", [((5000, 7), 0), ((100, 300), 1), ((33, 40, 5), 1), ((33, 40, 5), 2),
+                                       ((7, 9000), 0), ((20_000, 3), 0), ((3, 20_000), 1), ((1, 50_000), 1),
+                                       ((4097, 2), 0), ((2, 3, 4, 5), 3)])
+def test_along_dims(shape, dim):
+    n = int(np.prod(shape))
+    x = gen("f32", n, stream=73, dist="normal")
+    xd = dev_of("f32", x).reshape(tuple(reversed(shape)))
+    y = ak.ak_accumulate(xd, dim=dim).cpu().numpy()
+    assert_close_f32(y, oracle.scan(x, "f32", shape, dim), _mass_lines(x.astype(np.float64), shape, dim))
+    xi = gen("i64", n, stream=74)
+    y = ak.ak_accumulate(dev_of("i64", xi).reshape(tuple(reversed(shape))), dim=dim, op="max").cpu().numpy()
+    assert_exact(y, oracle.scan(xi, "i64", shape, dim, op="max"))
+    xm = synth.mat2_modp(n, stream=75)
+    xmd = dev_of("mat2", xm).reshape(tuple(reversed(shape)) + (4,))
+    y = ak.ak_accumulate(xmd, dim=dim, op="matmul", elem="mat2").cpu().numpy().view(np.uint32)
+    assert_exact(y.reshape(-1, 4), oracle.scan(xm, "mat2", shape, dim))
+
+
+# --------------------------------------------------------------------------
+# bounded waits
+# --------------------------------------------------------------------------
+
+def test_lookback_wait_runs_out_and_gpu_stays_usable():
+    # Tile 5 never publishes its state (fault injection); its successor's
+    # bounded wait runs out after 20 ms, the kernel records the failure and
+    # every block leaves. The call reports AK_ERR_TIMEOUT; the next call works.
+    x = gen("f64", 40 * 4096, stream=76)
+    xd = dev_of("f64", x)
+    opts = ak.make_opts(check=True, wait_limit_ns=20_000_000, debug_skip_publish_tile=5)
+    with pytest.raises(ak.AkError) as ei:
+        ak.ak_accumulate(xd, opts=opts)
+    assert ei.value.status == 6
+    y = ak.ak_accumulate(xd, opts=ak.make_opts(check=True)).cpu().numpy()
+    assert_close_f32(y, oracle.scan(x, "f64"), np.cumsum(np.abs(x)), rel=F64_REL)
