@@ -214,6 +214,35 @@ ak_status ak_accumulate(const void* src, void* dst, int ndim, const int64_t* sha
                         void* stream);
 
 /* ---------------------------------------------------------------------------
+ * ak_reduce_noalloc: ak_reduce for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that must not call cudaMalloc or any allocating routine when they reduce:
+ * a real-time loop that cannot afford the implicit device synchronisation
+ * of cudaMalloc / cudaFree, a process whose device memory is already fully
+ * reserved by another allocator, or code held to a fixed memory budget.
+ *
+ * Arguments, results, store and empty-input rules are those of ak_reduce;
+ * the caller still passes src and dst_dev / dst_host. The scratch (first-pass
+ * partials and the bare result slot) lives in a fixed array of
+ * AK_NOALLOC_SCRATCH_BYTES inside the library's device image, so every GPU
+ * that loads the library holds that much memory until the process exits. A
+ * call whose plan needs more scratch than that (it grows with the SM count
+ * and the partial size, about 20 KB on a 152-SM GPU) returns
+ * AK_ERR_WORKSPACE without launching anything.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture. Every call on a device shares the one array:
+ * calls that may overlap on the GPU (different streams, no ordering) race
+ * on it and give wrong results; order them on one stream. Nothing in the
+ * array needs clearing between calls.
+ * ------------------------------------------------------------------------- */
+#define AK_NOALLOC_SCRATCH_BYTES 65536
+ak_status ak_reduce_noalloc(const void* src, int64_t n, ak_dtype in, ak_map f, ak_op op, ak_dtype acc,
+                            ak_dtype out, const void* init, ak_store mode, void* dst_dev, void* dst_host,
+                            const ak_opts* opts, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Shape selector of ak_reduce_dims, exposed for inspection and tests (pure
  * host logic, no device needed). For a canonical strided problem of
  * `inner` contiguous outputs, reduction length `red_len` at stride `inner`

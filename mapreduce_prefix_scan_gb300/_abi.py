@@ -24,7 +24,7 @@ SHAPES = {"auto": 0, "thread": 1, "tiled": 2, "columns": 3}
 EXPORTS = ("ak_opts_default", "ak_status_string", "ak_dtype_size", "ak_last_cuda_error",
            "ak_kernel_launch_count", "ak_reduce_workspace_size", "ak_reduce",
            "ak_reduce_dims_workspace_size", "ak_reduce_dims", "ak_accumulate_workspace_size",
-           "ak_accumulate", "ak_dims_select")
+           "ak_accumulate", "ak_dims_select", "ak_reduce_noalloc")
 
 
 class ak_opts(ctypes.Structure):
@@ -68,8 +68,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ak_accumulate_workspace_size.argtypes = [I32, PI64, I32, I32, I32, I32, PO, PSZ]
     L.ak_accumulate.argtypes = [P, P, I32, PI64, I32, I32, I32, I32, I32, P, P, SZ, PO, P]
     L.ak_dims_select.argtypes = [I64, I64, I64, I32, I32, I32, I32, PI32, PI32, PI32, PI32]
+    L.ak_reduce_noalloc.argtypes = [P, I64, I32, I32, I32, I32, I32, P, I32, P, P, PO, P]
     for f in ("ak_reduce_workspace_size", "ak_reduce", "ak_reduce_dims_workspace_size", "ak_reduce_dims",
-              "ak_accumulate_workspace_size", "ak_accumulate", "ak_dims_select"):
+              "ak_accumulate_workspace_size", "ak_accumulate", "ak_dims_select", "ak_reduce_noalloc"):
         getattr(L, f).restype = I32
     _lib = L
     return L
