@@ -111,9 +111,10 @@ class ClockSampler:
 # our arm
 # ---------------------------------------------------------------------------
 
-def _traffic_from_profile(kernel_hash: str):
-    """DRAM bytes per launch of the whole-array first pass from the committed
-    ncu summary, if it was taken on the current kernel source."""
+def _traffic_from_profile(kernel_hash: str, algorithmic_bytes: float):
+    """DRAM bytes per launch of the whole-array reduce from the committed ncu
+    summary (traffic / algorithmic ratio x the algorithmic bytes), or None
+    when that capture was taken on an older kernel source."""
     path = os.path.join(ROOT, "profiles", "reduce_pass1_1e8.md")
     try:
         lines = open(path).read().splitlines()
@@ -127,7 +128,7 @@ def _traffic_from_profile(kernel_hash: str):
     if vals.get("kernel_source_sha256") != kernel_hash:
         return None
     try:
-        return float(vals["dram_bytes_per_launch_f32_abs2"])
+        return round(float(vals["traffic_over_algorithmic"]) * algorithmic_bytes)
     except (KeyError, ValueError):
         return None
 
@@ -383,8 +384,9 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "us_per_call": {k: round(v, 2) for k, v in per_call_us.items()},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": _traffic_from_profile(khash),
+                         "frac": round(achieved / peak, 4), "traffic": _traffic_from_profile(khash, step_bytes / len(calls)),
                          "kernel": "ak_reduce (first pass + one-block finish) on n=1e8",
+                         "achieved_basis": "bytes per ak_reduce call / its CUDA-event duration, mean over the step",
                          "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s"},
             "cpu_baseline": cpu,
@@ -470,6 +472,47 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(case: str):
+    """A few launches of one kernel family on a small case, for ncu captures
+    (the plain run of the same command must exit 0 first)."""
+    import torch
+
+    import mapreduce_prefix_scan_gb300 as ak
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if case == "reduce":  # 5e7 f32 abs2 sum: 200 MB, larger than L2
+        x = torch.from_numpy(synth.uniform_f32_pm1(5 * 10**7, 0, 2)).to(dev)
+        r = torch.empty(1, device=dev)
+        fn = lambda: ak.ak_reduce(x, f="abs2", dst=r)
+    elif case == "scan":  # 2e7 f64 cumsum: 160 MB in, 160 MB out
+        x = torch.from_numpy(synth.uniform_f64_01(2 * 10**7, 0, 60)).to(dev)
+        y = torch.empty_like(x)
+        fn = lambda: ak.ak_accumulate(x, dst=y)
+    elif case == "scan_max":  # 1e7 f32 max, Optional partials
+        x = torch.from_numpy(synth.normal_f32(10**7, 0, 61)).to(dev)
+        y = torch.empty_like(x)
+        o = ak.make_opts(no_neutral=True)
+        fn = lambda: ak.ak_accumulate(x, dst=y, op="max", opts=o)
+    elif case == "scan_mat2":  # 1e7 2x2 matrices mod p
+        x = torch.from_numpy(synth.mat2_modp(10**7, 0, 63)).to(dev)
+        y = torch.empty_like(x)
+        fn = lambda: ak.ak_accumulate(x, dst=y, op="matmul", elem="mat2")
+    elif case == "dims":  # 3072 x 2048 bf16, sum(x; dims=2)
+        x = torch.from_numpy(synth.normal_bf16_bits(3072 * 2048, 0, 40).view(np.int16)).view(torch.bfloat16)
+        x = x.reshape(2048, 3072).to(dev)
+        fn = lambda: ak.ak_reduce_dims(x, [1])
+    elif case == "dims_big":  # 8192 x 8192 f32, sum(x; dims=2)
+        x = torch.from_numpy(synth.normal_f32(8192 * 8192, 0, 40)).reshape(8192, 8192).to(dev)
+        fn = lambda: ak.ak_reduce_dims(x, [1])
+    else:
+        raise SystemExit(f"unknown profile case {case}")
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    print(f"profile case {case}: ok, {ak.ak_kernel_launch_count()} launches")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -479,9 +522,12 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload kernel numbers")
     ap.add_argument("--config-reps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
-    ap.add_argument("--small", action="store_true", help="n = 1e6 (for profiling captures)")
+    ap.add_argument("--small", action="store_true", help="n = 1e6 (quick runs)")
+    ap.add_argument("--profile", default=None, help="run a small ncu case: reduce|scan|scan_max|scan_mat2|dims|dims_big")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args.profile)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
