@@ -115,45 +115,82 @@ __device__ __forceinline__ bool aborted(const ScanCtl& ctl) {
     return ld_relaxed_u64(ctl.error_word) == ctl.epoch;
 }
 
-// Warp 0: exclusive prefix of tile g from its predecessors g_first..g-1.
-// Returns false when a wait ran out or another block gave up.
+// Ordered combine over the block (thread 0 leftmost) for a runtime block
+// size; the result is valid in thread 0; ends with the block in sync.
 template <class M>
-__device__ __forceinline__ bool look_back(int64_t g, int64_t g_first, const TileState<typename M::P>& ts,
-                          const ScanCtl& ctl, typename M::P* excl_out) {
+__device__ __forceinline__ typename M::P block_reduce_rt(typename M::P v, typename M::P* red, int W) {
+    const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
+    v = warp_reduce<M>(v);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        typename M::P w = lane < W ? red[lane] : M::empty();
+        v = warp_reduce<M>(w);
+    }
+    __syncthreads();
+    return v;
+}
+
+// Block-wide look-back: the exclusive prefix of tile g from its
+// predecessors g_first..g-1, valid in thread 0. Thread t inspects tile
+// hi - (B-1) + t, so one round covers B predecessors (a whole wave of the
+// persistent grid); rounds repeat only while no inclusive prefix is found.
+// Returns false (in every thread) when a wait ran out or another block gave
+// up.
+template <class M>
+__device__ __forceinline__ bool block_look_back(int64_t g, int64_t g_first, const TileState<typename M::P>& ts,
+                                                const ScanCtl& ctl, typename M::P* red, int* ints,
+                                                typename M::P* excl0) {
     using P = typename M::P;
-    const int lane = threadIdx.x % kWarp;
+    const int B = blockDim.x, W = B / kWarp;
+    const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
     P excl = M::empty();
     int64_t hi = g - 1;
     const uint64_t t_start = globaltimer_ns();
     while (true) {
-        const int64_t idx = hi - (kWarp - 1) + lane;  // lane 31 = nearest predecessor
+        const int64_t idx = hi - (B - 1) + tid;
         const bool valid = idx >= g_first;
         uint64_t status = 0;
-        while (true) {
-            if (valid) {
+        bool fail = false;
+        if (valid) {
+            while (true) {
                 const uint64_t f = ld_acquire_u64(ts.flags + idx);
                 status = (f >> 2) == ctl.epoch ? (f & 3u) : 0u;
+                if (status != 0) break;
+                if (globaltimer_ns() - t_start > (uint64_t)ctl.wait_limit_ns || aborted(ctl)) {
+                    fail = true;
+                    break;
+                }
+                __nanosleep(64);
             }
-            if (__all_sync(kFull, !valid || status != 0)) break;
-            bool give_up = false;
-            if (lane == 0) give_up = (globaltimer_ns() - t_start > (uint64_t)ctl.wait_limit_ns) || aborted(ctl);
-            if (__shfl_sync(kFull, give_up, 0)) return false;
-            __nanosleep(64);
         }
+        if (__syncthreads_or(fail)) return false;
+        // nearest inclusive prefix of the window: the highest thread holding one
         const unsigned pm = __ballot_sync(kFull, valid && status == kStatusPrefix);
-        const int stop = pm ? (kWarp - 1 - __clz(pm)) : -1;  // nearest lane holding an inclusive prefix
+        if (lane == 0) ints[warp] = pm ? warp * kWarp + (kWarp - 1 - __clz(pm)) : -1;
+        __syncthreads();
+        int stop = -1;
+        for (int w = 0; w < W; ++w) stop = max(stop, ints[w]);
         P v = M::empty();
-        if (valid && lane == stop) v = ld_coherent(ts.incls + idx);
-        else if (valid && lane > stop) v = ld_coherent(ts.aggs + idx);
-        v = warp_reduce<M>(v);          // lane 0: tiles in increasing order
-        v = shfl_idx_any(v, 0);
-        excl = M::combine(v, excl);
-        if (pm) break;
-        hi -= kWarp;
+        if (valid && tid == stop) v = ld_coherent(ts.incls + idx);
+        else if (valid && tid > stop) v = ld_coherent(ts.aggs + idx);
+        v = block_reduce_rt<M>(v, red, W);  // tiles in increasing order
+        if (tid == 0) excl = M::combine(v, excl);
+        if (stop >= 0) break;
+        hi -= B;
     }
-    *excl_out = excl;
+    if (tid == 0) *excl0 = excl;
     return true;
 }
+
+// cp.async (LDGSTS) 16-byte global -> shared copy, cached in L2 only.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global.L2::128B [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <class P>
 __device__ __forceinline__ void publish(const TileState<P>& ts, int64_t g, uint64_t status, const P& v,
@@ -163,29 +200,58 @@ __device__ __forceinline__ void publish(const TileState<P>& ts, int64_t g, uint6
     st_release_u64(ts.flags + g, (epoch << 2) | status);
 }
 
+template <class Acc>
+constexpr int scan_max_threads() { return sizeof(Acc) >= 16 ? 256 : 512; }
+
 // One tile scan over lines of `len` contiguous elements (lines follow each
-// other in memory). Dynamic shared memory: the padded run tile, then the
-// block-scan scratch.
+// other in memory). Dynamic shared memory: one padded run tile (two when the
+// next tile is prefetched), then the block-scan scratch. When the input and
+// accumulator types coincide, the block prefetches its next tile with
+// cp.async into the second buffer while it scans, looks back and stores
+// the current one.
 template <class In, class Acc, class Out, class M, int ITEMS>
-__global__ void __launch_bounds__(kMaxBlock) k_scan_tiles(const In* __restrict__ x, Out* __restrict__ y,
-                                                          int64_t len, int64_t tiles_per_line,
-                                                          int64_t ntiles, TileState<typename M::P> ts,
-                                                          ScanCtl ctl, bool has_init, Acc init) {
+__global__ void __launch_bounds__(scan_max_threads<Acc>(), 2)
+    k_scan_tiles(const In* __restrict__ x, Out* __restrict__ y, int64_t len, int64_t tiles_per_line, int64_t ntiles,
+                 TileState<typename M::P> ts, ScanCtl ctl, bool has_init, Acc init) {
     using P = typename M::P;
     using L = RunLayout<Acc, ITEMS>;
+    constexpr bool kPrefetch = std::is_same_v<In, Acc>;
     extern __shared__ __align__(16) char smem_raw[];
     const int B = blockDim.x;
     const int W = B / kWarp;
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
-    char* tile = smem_raw;
-    P* warp_tot = reinterpret_cast<P*>(smem_raw + (size_t)B * L::stride * 16);
-    P* bcast = warp_tot + kWarp;  // [0] block exclusive-of-warp base, [1] tile prefix
-    int* stop_flag = reinterpret_cast<int*>(bcast + 2);
+    const size_t tile_bytes = (size_t)B * L::stride * 16;
+    // buffer k of the (one or two) run tiles
+    auto buf_of = [&](int k) { return smem_raw + (kPrefetch ? (size_t)k * tile_bytes : 0); };
+    P* warp_tot = reinterpret_cast<P*>(smem_raw + (kPrefetch ? 2 : 1) * tile_bytes);
+    P* red = warp_tot + kWarp;
+    P* bcast = red + kWarp;  // [0] tile aggregate, [1] tile prefix
+    int* ints = reinterpret_cast<int*>(bcast + 2);  // [0..W) look-back scratch, [kWarp] stop flag
 
     const int tile_elems = B * ITEMS;
     constexpr int VIN = sizeof(In) < 16 ? 16 / (int)sizeof(In) : 1;   // input elements per 16-byte load
     constexpr int VOUT = sizeof(Out) < 16 ? 16 / (int)sizeof(Out) : 1;
     static_assert(ITEMS % VIN == 0 && ITEMS % VOUT == 0, "runs must hold whole vectors");
+
+    // Starts the asynchronous copy of tile gg into buf; false when gg does not
+    // exist or is ragged / unaligned (those are loaded synchronously).
+    auto prefetch = [&](int64_t gg, char* buf) -> bool {
+        if constexpr (!kPrefetch) {
+            return false;
+        } else {
+            if (gg >= ntiles) return false;
+            const int64_t t = gg % tiles_per_line;
+            if (len - t * (int64_t)tile_elems < tile_elems) return false;
+            const In* src = x + (gg / tiles_per_line) * len + t * tile_elems;
+            if (reinterpret_cast<uintptr_t>(src) % 16 != 0) return false;
+            for (int v = tid; v < tile_elems / VIN; v += B) cp_async16(buf + L::elem_off(v * VIN), src + (int64_t)v * VIN);
+            return true;
+        }
+    };
+
+    int cur = 0;
+    bool have = prefetch(blockIdx.x, buf_of(0));
+    if constexpr (kPrefetch) cp_async_commit();
 
     for (int64_t g = blockIdx.x; g < ntiles; g += gridDim.x) {
         const int64_t line = g / tiles_per_line, t = g % tiles_per_line;
@@ -193,29 +259,38 @@ __global__ void __launch_bounds__(kMaxBlock) k_scan_tiles(const In* __restrict__
         const int cnt = (int)min((int64_t)tile_elems, len - t * (int64_t)tile_elems);
         const In* src = x + start;
         Out* dst = y + start;
+        char* tile = buf_of(cur);
 
-        // ---- striped load into the padded run layout
-        const bool vec_in = cnt == tile_elems && (reinterpret_cast<uintptr_t>(src) % 16 == 0);
-        if (vec_in) {
-            for (int v = tid; v < tile_elems / VIN; v += B) {
-                In e[VIN];
-                if constexpr (VIN > 1) {
-                    Raw<16> r = ld_stream16(src + (int64_t)v * VIN);
-                    memcpy(e, &r, 16);
-                } else {
-                    e[0] = src[v];
-                }
-                Acc a[VIN];
+        bool have_next = false;
+        if constexpr (kPrefetch) {
+            have_next = prefetch(g + gridDim.x, buf_of(cur ^ 1));
+            cp_async_commit();
+            cp_async_wait<1>();  // this tile's group has landed (the newest may still fly)
+        }
+        // ---- striped load into the padded run layout (when not prefetched)
+        if (!have) {
+            const bool vec_in = cnt == tile_elems && (reinterpret_cast<uintptr_t>(src) % 16 == 0);
+            if (vec_in) {
+                for (int v = tid; v < tile_elems / VIN; v += B) {
+                    In e[VIN];
+                    if constexpr (VIN > 1) {
+                        Raw<16> r = ld_stream16(src + (int64_t)v * VIN);
+                        memcpy(e, &r, 16);
+                    } else {
+                        e[0] = src[v];
+                    }
+                    Acc a[VIN];
 #pragma unroll
-                for (int q = 0; q < VIN; ++q) a[q] = convert<Acc>(e[q]);
-                smem_store(tile + L::elem_off(v * VIN), a);
-            }
-        } else {
-            for (int e = tid; e < tile_elems; e += B) {
-                Acc a;
-                if (e < cnt) a = convert<Acc>(src[e]);
-                else memset(&a, 0, sizeof a);
-                *reinterpret_cast<Acc*>(tile + L::elem_off(e)) = a;
+                    for (int q = 0; q < VIN; ++q) a[q] = convert<Acc>(e[q]);
+                    smem_store(tile + L::elem_off(v * VIN), a);
+                }
+            } else {
+                for (int e = tid; e < tile_elems; e += B) {
+                    Acc a;
+                    if (e < cnt) a = convert<Acc>(src[e]);
+                    else memset(&a, 0, sizeof a);
+                    *reinterpret_cast<Acc*>(tile + L::elem_off(e)) = a;
+                }
             }
         }
         __syncthreads();
@@ -249,35 +324,33 @@ __global__ void __launch_bounds__(kMaxBlock) k_scan_tiles(const In* __restrict__
             P wi = warp_inclusive_scan<M>(w, lane);
             P we = shfl_up_any(wi, 1);
             if (lane == 0) we = M::empty();
-            if (lane < W) warp_tot[lane] = we;          // exclusive base of each warp
-            P agg = shfl_idx_any(wi, W - 1);              // tile aggregate
-
-            // ---- tile prefix
-            P prefix = M::empty();
-            int stop = 0;
-            const bool first = (t == 0);
-            const bool last = (t == tiles_per_line - 1);
-            const bool skip = (g == ctl.skip_tile);
-            if (first) {
-                if (has_init) prefix = M::lift(init);
-                if (!last && lane == 0 && !skip) publish(ts, g, kStatusPrefix, M::combine(prefix, agg), ctl.epoch);
-            } else {
-                if (!last && lane == 0 && !skip) publish(ts, g, kStatusAggregate, agg, ctl.epoch);
-                if (!look_back<M>(g, g - t, ts, ctl, &prefix)) {
-                    stop = 1;
-                    if (lane == 0) atomicExch(reinterpret_cast<unsigned long long*>(ctl.error_word),
-                                              (unsigned long long)ctl.epoch);
-                } else if (!last && lane == 0 && !skip) {
-                    publish(ts, g, kStatusPrefix, M::combine(prefix, agg), ctl.epoch);
-                }
-            }
-            if (lane == 0) {
-                bcast[1] = prefix;
-                *stop_flag = stop;
-            }
+            if (lane < W) warp_tot[lane] = we;  // exclusive base of each warp
+            if (lane == 0) bcast[0] = shfl_idx_any(wi, W - 1);
+            else shfl_idx_any(wi, W - 1);
         }
         __syncthreads();
-        if (*stop_flag) return;  // uniform: every thread read the same flag
+
+        // ---- tile prefix: publish the aggregate, look back, publish the prefix
+        const P agg = bcast[0];
+        const bool first = (t == 0);
+        const bool last = (t == tiles_per_line - 1);
+        const bool skip = (g == ctl.skip_tile);
+        P prefix = M::empty();
+        if (first) {
+            if (has_init) prefix = M::lift(init);
+            if (tid == 0 && !last && !skip) publish(ts, g, kStatusPrefix, M::combine(prefix, agg), ctl.epoch);
+        } else {
+            if (tid == 0 && !last && !skip) publish(ts, g, kStatusAggregate, agg, ctl.epoch);
+            if (!block_look_back<M>(g, g - t, ts, ctl, red, ints, &prefix)) {
+                if (tid == 0)
+                    atomicExch(reinterpret_cast<unsigned long long*>(ctl.error_word), (unsigned long long)ctl.epoch);
+                if constexpr (kPrefetch) cp_async_wait<0>();  // no copy may outlive the block
+                return;  // uniform: every thread got the same answer
+            }
+            if (tid == 0 && !last && !skip) publish(ts, g, kStatusPrefix, M::combine(prefix, agg), ctl.epoch);
+        }
+        if (tid == 0) bcast[1] = prefix;
+        __syncthreads();
 
         // ---- apply prefixes to the run, write back
         const P base = M::combine(M::combine(bcast[1], warp_tot[warp]), lane_excl);
@@ -308,8 +381,11 @@ __global__ void __launch_bounds__(kMaxBlock) k_scan_tiles(const In* __restrict__
                 dst[e] = convert<Out>(*reinterpret_cast<const Acc*>(tile + L::elem_off(e)));
             }
         }
-        __syncthreads();  // the tile buffer is reused by the next tile
+        __syncthreads();  // this buffer is refilled two tiles later
+        have = have_next;
+        cur ^= 1;
     }
+    if constexpr (kPrefetch) cp_async_wait<0>();
 }
 
 // Lines along a strided dimension: y[i + I*(j + J*k)] over j, for every
@@ -343,10 +419,11 @@ __global__ void __launch_bounds__(256) k_scan_strided(const In* __restrict__ x, 
     }
 }
 
-template <class Acc, class M>
+template <class In, class Acc, class M>
 size_t tile_smem_bytes(int block) {
     using L = RunLayout<Acc, default_items<Acc>()>;
-    return (size_t)block * L::stride * 16 + (kWarp + 2) * sizeof(typename M::P) + 16;
+    const size_t bufs = std::is_same_v<In, Acc> ? 2 : 1;
+    return bufs * block * L::stride * 16 + (2 * kWarp + 2) * sizeof(typename M::P) + (kWarp + 4) * sizeof(int);
 }
 
 template <class In, class Acc, class Out, class M>
@@ -369,7 +446,7 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
         return AK_ERR_UNSUPPORTED;
     } else {
         auto kernel = k_scan_tiles<In, Acc, Out, M, ITEMS>;
-        const size_t smem = tile_smem_bytes<Acc, M>(p.block);
+        const size_t smem = tile_smem_bytes<In, Acc, M>(p.block);
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return cuda_fail(e);
         int occ = 0;
@@ -430,9 +507,10 @@ ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_d
     p->items = it;
     // Block size: the smallest of 128 / 256 / 512 threads whose tile holds a
     // whole line, else 512 (fewer, larger tiles for long lines).
-    int block = kMaxBlock;
+    const int max_block = asz >= 16 ? 256 : kMaxBlock;
+    int block = max_block;
     for (int b : {128, 256, 512}) {
-        if ((int64_t)b * it >= len) { block = b; break; }
+        if (b <= max_block && (int64_t)b * it >= len) { block = b; break; }
     }
     p->block = block;
     const int64_t tile = (int64_t)block * it;
