@@ -55,6 +55,49 @@ __device__ __forceinline__ T raw_get(const Raw<BYTES>& r, int k) {
     return v;
 }
 
+// L2 eviction-priority policies (createpolicy) and 16-byte accesses that
+// carry them: evict_last keeps a tile in L2 until it is read again,
+// evict_first marks a last use.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ Raw<16> ld_hint16(const void* p, uint64_t policy) {
+    Raw<16> r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
+                 : "l"(p), "l"(policy));
+    return r;
+}
+__device__ __forceinline__ void st_hint16(void* p, const Raw<16>& r, uint64_t policy) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(r.w[0]),
+                 "r"(r.w[1]), "r"(r.w[2]), "r"(r.w[3]), "l"(policy)
+                 : "memory");
+}
+
+// 32-byte (sm_100+ 256-bit) load / store with an L2 policy: one lane's
+// access covers a whole 32-byte sector.
+__device__ __forceinline__ Raw<32> ld_hint32(const void* p, uint64_t policy) {
+    Raw<32> r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]), "=r"(r.w[5]),
+                   "=r"(r.w[6]), "=r"(r.w[7])
+                 : "l"(p), "l"(policy));
+    return r;
+}
+__device__ __forceinline__ void st_hint32(void* p, const Raw<32>& r, uint64_t policy) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;" ::"l"(p),
+                 "r"(r.w[0]), "r"(r.w[1]), "r"(r.w[2]), "r"(r.w[3]), "r"(r.w[4]), "r"(r.w[5]), "r"(r.w[6]),
+                 "r"(r.w[7]), "l"(policy)
+                 : "memory");
+}
+
 // Plain 16-byte global store that does not allocate in L1.
 __device__ __forceinline__ void st_global16(void* p, const Raw<16>& r) {
     asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(r.w[0]),

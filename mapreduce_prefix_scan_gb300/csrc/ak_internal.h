@@ -210,7 +210,8 @@ struct ScanCall {
     cudaStream_t stream;
 };
 struct ScanPlan {
-    int kind;        // 0 = tile scan of contiguous lines, 1 = strided (inner > 1)
+    int kind;        // 0 = super-tile scan of long contiguous lines, 1 = strided (inner > 1),
+                     // 2 = contiguous lines that fit one tile
     int block, items;
     int grid;
     int64_t tiles_per_line, tiles;

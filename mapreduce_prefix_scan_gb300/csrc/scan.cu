@@ -19,14 +19,17 @@
 // Garland, "Single-pass Parallel Prefix Scan with Decoupled Look-back",
 // 2016): a tile publishes its aggregate, a warp inspects up to 32
 // predecessors at a time, folds aggregates back to the nearest published
-// inclusive prefix, then publishes its own inclusive prefix. The grid is
-// persistent and cooperative (all blocks co-resident) and each block takes
-// its tiles in increasing order, so the lowest unfinished tile can always
-// progress. Every tile-state word carries the call's epoch, so stale state
-// from earlier calls is never mistaken for a publication and the workspace
-// needs no clearing. Every wait is bounded by a global-timer deadline; a
-// block that gives up records the epoch in the workspace's error word,
-// which every other waiter also watches, and all blocks leave early.
+// inclusive prefix, then publishes its own inclusive prefix. One block per
+// tile, several blocks per SM, so one tile's look-back hides behind other
+// tiles' loads. A block takes its tile index from an atomic counter when it
+// starts, so every tile it waits for belongs to a block that is already
+// running: progress never depends on the order in which the hardware
+// dispatches blocks. The counter and every tile-state word carry the call's
+// epoch, so stale state from earlier calls is never mistaken for current
+// state and the workspace needs no clearing. Every wait is bounded by a
+// global-timer deadline; a block that gives up records the epoch in the
+// workspace's error word, which every other waiter also watches, and all
+// blocks leave early.
 #include <algorithm>
 
 #include "ak_common.cuh"
@@ -36,13 +39,33 @@ namespace ak {
 
 namespace {
 
-constexpr int kMaxBlock = 512;
 constexpr unsigned kFull = 0xffffffffu;
 enum : uint64_t { kStatusAggregate = 1, kStatusPrefix = 2 };
 
+// Run length (items per thread) and block size per accumulator size: 128-byte
+// runs, 32 KB tiles for 4- and 8-byte elements (16 KB for 16-byte ones).
 template <class Acc>
 constexpr int default_items() {
-    return sizeof(Acc) >= 16 ? 8 : (sizeof(Acc) == 8 ? 8 : 16);
+    return sizeof(Acc) >= 16 ? 8 : (sizeof(Acc) == 8 ? 16 : 32);
+}
+template <class Acc>
+constexpr int default_block() {
+    return sizeof(Acc) >= 16 ? 128 : 256;
+}
+// Elements of one thread's segment in the long-line scan: 512 bytes of
+// 4- and 8-byte elements, 1 KB of 16-byte ones (128 KB super-tiles).
+template <class Acc>
+constexpr int default_seg() {
+    return sizeof(Acc) >= 16 ? 64 : (sizeof(Acc) == 8 ? 64 : 128);
+}
+// Predecessor super-tiles one look-back round inspects, per thread.
+constexpr int kLookSlots = 2;
+// Resident blocks per SM the register budget is sized for: 3 blocks of 256
+// threads (<= 80 registers a thread), a quarter of the thread slots for
+// 16-byte elements.
+template <int BLOCK, int ACC_BYTES>
+constexpr int min_blocks_per_sm() {
+    return ACC_BYTES >= 16 ? 2048 / BLOCK / 4 : 3;
 }
 
 // Shared-memory run layout: run r starts at 16-byte chunk r * run_stride.
@@ -58,8 +81,6 @@ struct RunLayout {
     }
 };
 
-// Copies of whole 16-byte chunks through uint4, so shared-memory traffic is
-// 128-bit (both pointers 16-byte aligned).
 // Register side is assembled word by word with compile-time indices so
 // that it stays in registers.
 template <class T, int N>
@@ -97,16 +118,68 @@ __device__ __forceinline__ void smem_store(char* dst, const T (&src)[N]) {
     }
 }
 
+// Tile state without fences: one record per super-tile, rewritten when the
+// aggregate is upgraded to the inclusive prefix. A record is written with
+// relaxed stores and accepted by a reader only when its tag carries this
+// call's epoch and its check word matches the tag and value read with it,
+// so a record from an earlier call, arbitrary memory, or a half-visible
+// rewrite is rejected and read again (a false acceptance needs a 64-bit
+// check collision). Status and value arrive in one read.
+template <class P>
+struct alignas(16) TileRec {
+    uint64_t tag;  // (epoch << 2) | status
+    uint64_t chk;
+    P v;
+};
+
 template <class P>
 struct TileState {
-    uint64_t* flags;
-    P* aggs;
-    P* incls;
+    TileRec<P>* recs;
 };
+
+template <class P>
+__device__ __forceinline__ uint64_t rec_check(uint64_t tag, const P& v) {
+    uint64_t h = tag * 0x9E3779B97F4A7C15ull;
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(P) / 4); ++i) {
+        h = (h ^ w[i]) * 0xBF58476D1CE4E5B9ull;
+        h ^= h >> 31;
+    }
+    return h ^ (h >> 29);
+}
+
+// Relaxed, L2-coherent word access of the records (never cached in L1, never
+// hoisted out of a polling loop).
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Reads a record: its status for this call (0 when not valid) and value.
+template <class P>
+__device__ __forceinline__ uint64_t read_rec(const TileRec<P>* r, uint64_t epoch, P* v) {
+    const uint64_t tag = ld_relaxed_u64(&r->tag);
+    const uint64_t chk = ld_relaxed_u64(&r->chk);
+    uint32_t* w = reinterpret_cast<uint32_t*>(v);
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(&r->v);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(P) / 4); ++i) w[i] = ld_relaxed_u32(src + i);
+    if ((tag >> 2) != epoch || chk != rec_check(tag, *v)) return 0;
+    return tag & 3u;
+}
 
 struct ScanCtl {
     uint64_t epoch;
     uint64_t* error_word;
+    unsigned long long* counter;  // tile claims: [0] tag (epoch << 1 | ready), [1] next index
     int64_t wait_limit_ns;
     int64_t skip_tile;  // fault injection; -1 = off
 };
@@ -115,10 +188,40 @@ __device__ __forceinline__ bool aborted(const ScanCtl& ctl) {
     return ld_relaxed_u64(ctl.error_word) == ctl.epoch;
 }
 
-// Ordered combine over the block (thread 0 leftmost) for a runtime block
-// size; the result is valid in thread 0; ends with the block in sync.
-template <class M>
-__device__ __forceinline__ typename M::P block_reduce_rt(typename M::P v, typename M::P* red, int W) {
+// The next tile index of this call. Two header words: `tag` says which call
+// owns the count and whether it has been reset, `count` hands out indices.
+// The first block of a call that sees a stale tag (an earlier call, or
+// uninitialised memory) wins a compare-and-swap to "resetting", zeroes the
+// count, and releases the tag as "ready"; every other block waits (bounded)
+// for "ready" and then takes an index with one atomic add. Returns ntiles
+// when the wait runs out (the block then does nothing).
+__device__ __forceinline__ int64_t claim_tile(const ScanCtl& ctl, int64_t ntiles) {
+    const unsigned long long resetting = (unsigned long long)ctl.epoch << 1;
+    const unsigned long long ready = resetting | 1ull;
+    unsigned long long* tag = ctl.counter;
+    unsigned long long* count = ctl.counter + 1;
+    // The winner's count reset is performed at L2 before its tag store is
+    // issued, so a block that sees "ready" and then adds at L2 sees the reset.
+    unsigned long long a = ld_relaxed_u64(reinterpret_cast<uint64_t*>(tag));
+    if (a == ready) return (int64_t)atomicAdd(count, 1ull);
+    if (a != resetting && atomicCAS(tag, a, resetting) == a) {
+        atomicExch(count, 1ull);  // index 0 is ours
+        st_relaxed_u64(reinterpret_cast<uint64_t*>(tag), ready);
+        return 0;
+    }
+    const uint64_t t_start = globaltimer_ns();
+    while (ld_relaxed_u64(reinterpret_cast<uint64_t*>(tag)) != ready) {
+        if (globaltimer_ns() - t_start > (uint64_t)ctl.wait_limit_ns) return ntiles;
+        __nanosleep(64);
+    }
+    return (int64_t)atomicAdd(count, 1ull);
+}
+
+// Ordered combine over the block (thread 0 leftmost); result in thread 0;
+// ends with the block in sync.
+template <class M, int BLOCK>
+__device__ __forceinline__ typename M::P block_reduce_ordered(typename M::P v, typename M::P* red) {
+    constexpr int W = BLOCK / kWarp;
     const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
     v = warp_reduce<M>(v);
     if (lane == 0) red[warp] = v;
@@ -131,261 +234,479 @@ __device__ __forceinline__ typename M::P block_reduce_rt(typename M::P v, typena
     return v;
 }
 
-// Block-wide look-back: the exclusive prefix of tile g from its
-// predecessors g_first..g-1, valid in thread 0. Thread t inspects tile
-// hi - (B-1) + t, so one round covers B predecessors (a whole wave of the
-// persistent grid); rounds repeat only while no inclusive prefix is found.
-// Returns false (in every thread) when a wait ran out or another block gave
-// up.
-template <class M>
-__device__ __forceinline__ bool block_look_back(int64_t g, int64_t g_first, const TileState<typename M::P>& ts,
-                                                const ScanCtl& ctl, typename M::P* red, int* ints,
-                                                typename M::P* excl0) {
+// Whole block: exclusive prefix of tile g from its predecessors
+// g_first..g-1, valid in thread 0. One round inspects the window of
+// kLookSlots * BLOCK tiles ending at hi (thread t holds the kLookSlots
+// consecutive tiles at 2t, 2t+1 of the window). A round first reads every
+// flag once and finds the nearest inclusive prefix, then waits only for the
+// tiles newer than it that have not published yet; with none in the window,
+// it waits for all of them, folds their aggregates and moves one window
+// back. The window is wide enough that the published-prefix frontier keeps
+// up with the rate at which tiles start. Returns false (in every thread)
+// when a wait ran out or another block gave up.
+template <class M, int BLOCK>
+__device__ __forceinline__ bool look_back(int64_t g, int64_t g_first, const TileState<typename M::P>& ts,
+                                          const ScanCtl& ctl, typename M::P* red, int* ints,
+                                          typename M::P* excl0) {
     using P = typename M::P;
-    const int B = blockDim.x, W = B / kWarp;
+    constexpr int W = BLOCK / kWarp, S = kLookSlots, WIN = S * BLOCK;
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    // Fast path: warp 0 reads the 32 nearest records once; when an inclusive
+    // prefix is among them and every newer one has published, that decides.
+    if (warp == 0) {
+        const int64_t idx = g - kWarp + lane;
+        const bool valid = idx >= g_first;
+        P val = M::empty();
+        const uint64_t st = valid ? read_rec(ts.recs + idx, ctl.epoch, &val) : 0;
+        const unsigned pm = __ballot_sync(kFull, valid && st == kStatusPrefix);
+        const int stop = pm ? (kWarp - 1 - __clz(pm)) : -1;
+        const bool ok = stop >= 0 && __ballot_sync(kFull, valid && lane > stop && st == 0) == 0;
+        if (ok) {
+            P v = (valid && lane >= stop) ? val : M::empty();
+            v = warp_reduce<M>(v);
+            if (lane == 0) *excl0 = v;
+        }
+        if (lane == 0) ints[2 * kWarp] = ok;
+    }
+    __syncthreads();
+    if (ints[2 * kWarp]) return true;
+
     P excl = M::empty();
     int64_t hi = g - 1;
     const uint64_t t_start = globaltimer_ns();
     while (true) {
-        const int64_t idx = hi - (B - 1) + tid;
-        const bool valid = idx >= g_first;
-        uint64_t status = 0;
+        const int64_t base = hi - (WIN - 1) + (int64_t)S * tid;  // this thread's first slot
+        uint64_t st[S];
+        P val[S];
+#pragma unroll
+        for (int k = 0; k < S; ++k) {
+            st[k] = 0;
+            val[k] = M::empty();
+            if (base + k >= g_first) st[k] = read_rec(ts.recs + base + k, ctl.epoch, &val[k]);
+        }
+        // nearest inclusive prefix seen so far: the highest window position
+        int mine = -1;
+#pragma unroll
+        for (int k = 0; k < S; ++k)
+            if (base + k >= g_first && st[k] == kStatusPrefix) mine = S * tid + k;
+        for (int d = kWarp / 2; d > 0; d >>= 1) mine = max(mine, __shfl_xor_sync(kFull, mine, d));
+        if (lane == 0) ints[warp] = mine;
+        __syncthreads();
+        int stop0 = -1;
+#pragma unroll
+        for (int w = 0; w < W; ++w) stop0 = max(stop0, ints[w]);
+        // wait for the unpublished tiles newer than it
         bool fail = false;
-        if (valid) {
-            while (true) {
-                const uint64_t f = ld_acquire_u64(ts.flags + idx);
-                status = (f >> 2) == ctl.epoch ? (f & 3u) : 0u;
-                if (status != 0) break;
-                if (globaltimer_ns() - t_start > (uint64_t)ctl.wait_limit_ns || aborted(ctl)) {
-                    fail = true;
-                    break;
+#pragma unroll
+        for (int k = 0; k < S; ++k) {
+            const int pos = S * tid + k;
+            if (base + k >= g_first && pos > stop0 && st[k] == 0) {
+                while (true) {
+                    st[k] = read_rec(ts.recs + base + k, ctl.epoch, &val[k]);
+                    if (st[k] != 0) break;
+                    if (globaltimer_ns() - t_start > (uint64_t)ctl.wait_limit_ns || aborted(ctl)) {
+                        fail = true;
+                        break;
+                    }
+                    __nanosleep(32);
                 }
-                __nanosleep(64);
             }
         }
         if (__syncthreads_or(fail)) return false;
-        // nearest inclusive prefix of the window: the highest thread holding one
-        const unsigned pm = __ballot_sync(kFull, valid && status == kStatusPrefix);
-        if (lane == 0) ints[warp] = pm ? warp * kWarp + (kWarp - 1 - __clz(pm)) : -1;
+        // a newer tile may have published its prefix meanwhile: use the nearest
+        mine = -1;
+#pragma unroll
+        for (int k = 0; k < S; ++k)
+            if (base + k >= g_first && S * tid + k >= stop0 && st[k] == kStatusPrefix) mine = S * tid + k;
+        for (int d = kWarp / 2; d > 0; d >>= 1) mine = max(mine, __shfl_xor_sync(kFull, mine, d));
+        if (lane == 0) ints[kWarp + warp] = mine;
         __syncthreads();
         int stop = -1;
-        for (int w = 0; w < W; ++w) stop = max(stop, ints[w]);
+#pragma unroll
+        for (int w = 0; w < W; ++w) stop = max(stop, ints[kWarp + w]);
+        // fold the window from the prefix (or its start) to its end, in order
         P v = M::empty();
-        if (valid && tid == stop) v = ld_coherent(ts.incls + idx);
-        else if (valid && tid > stop) v = ld_coherent(ts.aggs + idx);
-        v = block_reduce_rt<M>(v, red, W);  // tiles in increasing order
+#pragma unroll
+        for (int k = 0; k < S; ++k) {
+            const int pos = S * tid + k;
+            if (base + k < g_first || pos < stop) continue;
+            v = M::combine(v, val[k]);
+        }
+        v = block_reduce_ordered<M, BLOCK>(v, red);
         if (tid == 0) excl = M::combine(v, excl);
-        if (stop >= 0) break;
-        hi -= B;
+        if (stop >= 0 || hi - WIN < g_first) break;
+        hi -= WIN;
     }
     if (tid == 0) *excl0 = excl;
     return true;
 }
 
-// cp.async (LDGSTS) 16-byte global -> shared copy, cached in L2 only.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global.L2::128B [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 template <class P>
 __device__ __forceinline__ void publish(const TileState<P>& ts, int64_t g, uint64_t status, const P& v,
                                         uint64_t epoch) {
-    if (status == kStatusAggregate) ts.aggs[g] = v;
-    else ts.incls[g] = v;
-    st_release_u64(ts.flags + g, (epoch << 2) | status);
+    TileRec<P>* r = ts.recs + g;
+    const uint64_t tag = (epoch << 2) | status;
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(&r->v);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(P) / 4); ++i) st_relaxed_u32(dst + i, w[i]);
+    st_relaxed_u64(&r->chk, rec_check(tag, v));
+    st_relaxed_u64(&r->tag, tag);
 }
 
-template <class Acc>
-constexpr int scan_max_threads() { return sizeof(Acc) >= 16 ? 256 : 512; }
+// ---------------------------------------------------------------------------
+// tile building blocks
+// ---------------------------------------------------------------------------
 
-// One tile scan over lines of `len` contiguous elements (lines follow each
-// other in memory). Dynamic shared memory: one padded run tile (two when the
-// next tile is prefetched), then the block-scan scratch. When the input and
-// accumulator types coincide, the block prefetches its next tile with
-// cp.async into the second buffer while it scans, looks back and stores
-// the current one.
-template <class In, class Acc, class Out, class M, int ITEMS>
-__global__ void __launch_bounds__(scan_max_threads<Acc>(), 2)
+// Striped (coalesced) load of one tile into the padded run layout, with the
+// given L2 policy; a ragged or unaligned tile is loaded element by element
+// and padded with zero bytes.
+template <class In, class Acc, int ITEMS, int BLOCK>
+__device__ __forceinline__ void load_tile(char* tile, const In* src, int cnt, uint64_t policy) {
+    using L = RunLayout<Acc, ITEMS>;
+    constexpr int TILE = BLOCK * ITEMS;
+    constexpr int VIN = sizeof(In) < 16 ? 16 / (int)sizeof(In) : 1;
+    static_assert(ITEMS % VIN == 0, "runs must hold whole vectors");
+    const int tid = threadIdx.x;
+    if (cnt == TILE && reinterpret_cast<uintptr_t>(src) % 16 == 0) {
+#pragma unroll
+        for (int k = 0; k < TILE / VIN / BLOCK; ++k) {
+            const int v = tid + k * BLOCK;
+            In e[VIN];
+            Raw<16> r = ld_hint16(src + (int64_t)v * VIN, policy);
+            memcpy(e, &r, sizeof e);
+            Acc a[VIN];
+#pragma unroll
+            for (int q = 0; q < VIN; ++q) a[q] = convert<Acc>(e[q]);
+            smem_store(tile + L::elem_off(v * VIN), a);
+        }
+    } else {
+        for (int e = tid; e < TILE; e += BLOCK) {
+            Acc a;
+            if (e < cnt) a = convert<Acc>(src[e]);
+            else memset(&a, 0, sizeof a);
+            *reinterpret_cast<Acc*>(tile + L::elem_off(e)) = a;
+        }
+    }
+}
+
+// Scan of the tile in shared memory with the tile's exclusive prefix
+// (`*prefix`, shared), then the coalesced store of the result; `*prefix`
+// then becomes the inclusive prefix of the tile (the next tile's carry).
+template <class Acc, class Out, class M, int ITEMS, int BLOCK>
+__device__ __forceinline__ void scan_apply_store(char* tile, Out* dst, int cnt, typename M::P* prefix,
+                                                 typename M::P* warp_tot, uint64_t policy) {
+    using P = typename M::P;
+    using L = RunLayout<Acc, ITEMS>;
+    constexpr int W = BLOCK / kWarp;
+    constexpr int TILE = BLOCK * ITEMS;
+    constexpr int VOUT = sizeof(Out) < 16 ? 16 / (int)sizeof(Out) : 1;
+    static_assert(ITEMS % VOUT == 0, "runs must hold whole vectors");
+    const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+
+    // each thread scans its run in registers
+    Acc run[ITEMS];
+    smem_load(run, L::run_ptr(tile, tid));
+#pragma unroll
+    for (int i = 1; i < ITEMS; ++i) run[i] = M::op::apply(run[i - 1], run[i]);
+    const int valid_items = min(ITEMS, max(0, cnt - tid * ITEMS));
+    P total = M::lift(run[ITEMS - 1]);
+    if (valid_items < ITEMS) {
+        // ragged run: predicated fold of the valid elements (still in smem)
+        Acc orig[ITEMS];
+        smem_load(orig, L::run_ptr(tile, tid));
+        total = M::empty();
+#pragma unroll
+        for (int i = 0; i < ITEMS; ++i)
+            if (i < valid_items) total = M::combine(total, M::lift(orig[i]));
+    }
+    // block scan of run totals (thread order)
+    P inc = warp_inclusive_scan<M>(total, lane);
+    P lane_excl = shfl_up_any(inc, 1);
+    if (lane == 0) lane_excl = M::empty();
+    if (lane == kWarp - 1) warp_tot[warp] = inc;
+    __syncthreads();
+    P block_total = M::empty();  // meaningful in warp 0
+    if (warp == 0) {
+        P w = lane < W ? warp_tot[lane] : M::empty();
+        P wi = warp_inclusive_scan<M>(w, lane);
+        P we = shfl_up_any(wi, 1);
+        if (lane == 0) we = M::empty();
+        if (lane < W) warp_tot[lane] = M::combine(*prefix, we);  // tile prefix + exclusive base of each warp
+        block_total = shfl_idx_any(wi, W - 1);
+    }
+    __syncthreads();
+    // apply the prefixes to the run, write back
+    const P base = M::combine(warp_tot[warp], lane_excl);
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) run[i] = M::value(M::combine(base, M::lift(run[i])));
+    smem_store(L::run_ptr(tile, tid), run);
+    __syncthreads();
+    // striped (coalesced) store
+    if (cnt == TILE && reinterpret_cast<uintptr_t>(dst) % 16 == 0) {
+#pragma unroll
+        for (int k = 0; k < TILE / VOUT / BLOCK; ++k) {
+            const int v = tid + k * BLOCK;
+            Acc a[VOUT];
+            smem_load(a, tile + L::elem_off(v * VOUT));
+            Out o[VOUT];
+#pragma unroll
+            for (int q = 0; q < VOUT; ++q) o[q] = convert<Out>(a[q]);
+            Raw<16> r;
+            memcpy(&r, o, 16);
+            st_hint16(dst + (int64_t)v * VOUT, r, policy);
+        }
+    } else {
+        for (int e = tid; e < cnt; e += BLOCK) dst[e] = convert<Out>(*reinterpret_cast<const Acc*>(tile + L::elem_off(e)));
+    }
+    if (tid == 0) *prefix = M::combine(*prefix, block_total);  // carry into the next sub-tile
+    __syncthreads();  // the tile buffer and the carry are used next
+}
+
+// ---------------------------------------------------------------------------
+// kernels
+// ---------------------------------------------------------------------------
+
+// ---------------------------------------------------------------------------
+// register-resident segments
+// ---------------------------------------------------------------------------
+
+// Each thread of a super-tile owns one contiguous segment of SEG elements,
+// read and written with 32-byte (256-bit) per-lane accesses: every access
+// is a whole sector, so a warp's blocked accesses use each DRAM / L2 sector
+// fully and no shared-memory transpose is needed.
+template <class In>
+__host__ __device__ constexpr int chunk_elems() {
+    return 32 / (int)sizeof(In);
+}
+
+// Fold of one segment (n <= SEG valid elements) in element order.
+template <class In, class M, int SEG>
+__device__ __forceinline__ typename M::P segment_fold(const In* src, int n, uint64_t policy) {
+    using P = typename M::P;
+    using Acc = typename M::acc;
+    constexpr int CH = chunk_elems<In>();
+    constexpr int NC = SEG / CH;
+    constexpr int U = NC < 8 ? NC : 8;
+    static_assert(SEG % CH == 0 && NC % U == 0, "whole chunks per segment");
+    if (n == SEG && reinterpret_cast<uintptr_t>(src) % 32 == 0) {
+        if constexpr (M::commutative) {
+            // one accumulator per chunk position: short dependency chains
+            P acc[CH];
+#pragma unroll
+            for (int q = 0; q < CH; ++q) acc[q] = M::empty();
+#pragma unroll 1
+            for (int c0 = 0; c0 < NC; c0 += U) {
+                Raw<32> r[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) r[u] = ld_hint32(src + (c0 + u) * CH, policy);
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int q = 0; q < CH; ++q)
+                        acc[q] = M::combine(acc[q], M::lift(convert<Acc>(raw_get<In>(r[u], q))));
+            }
+            P a = acc[0];
+#pragma unroll
+            for (int q = 1; q < CH; ++q) a = M::combine(a, acc[q]);
+            return a;
+        } else {
+            P a = M::empty();
+#pragma unroll 1
+            for (int c0 = 0; c0 < NC; c0 += U) {
+                Raw<32> r[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) r[u] = ld_hint32(src + (c0 + u) * CH, policy);
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int q = 0; q < CH; ++q) a = M::combine(a, M::lift(convert<Acc>(raw_get<In>(r[u], q))));
+            }
+            return a;
+        }
+    }
+    P a = M::empty();
+    for (int i = 0; i < n; ++i) a = M::combine(a, M::lift(convert<Acc>(src[i])));
+    return a;
+}
+
+// Stores the CH outputs of one chunk (CH * sizeof(Out) bytes: 16, 32 or 64).
+template <class Out, int CH>
+__device__ __forceinline__ void store_chunk(Out* dst, const Out (&o)[CH], uint64_t policy) {
+    constexpr int NB = CH * (int)sizeof(Out);
+    if constexpr (NB == 16) {
+        Raw<16> r;
+        memcpy(&r, o, 16);
+        st_hint16(dst, r, policy);
+    } else {
+        static_assert(NB % 32 == 0, "chunk of whole sectors");
+#pragma unroll
+        for (int h = 0; h < NB / 32; ++h) {
+            Raw<32> r;
+            memcpy(&r, reinterpret_cast<const char*>(o) + 32 * h, 32);
+            st_hint32(reinterpret_cast<char*>(dst) + 32 * h, r, policy);
+        }
+    }
+}
+
+// Inclusive scan of one segment starting from the exclusive prefix `acc`,
+// stored to dst.
+template <class In, class Out, class M, int SEG>
+__device__ __forceinline__ void segment_scan_store(const In* src, Out* dst, int n, typename M::P acc,
+                                                   uint64_t pol_in, uint64_t pol_out) {
+    using Acc = typename M::acc;
+    constexpr int CH = chunk_elems<In>();
+    constexpr int NC = SEG / CH;
+    constexpr int U = NC < 8 ? NC : 8;
+    constexpr int OB = CH * (int)sizeof(Out);
+    if (n == SEG && reinterpret_cast<uintptr_t>(src) % 32 == 0 &&
+        reinterpret_cast<uintptr_t>(dst) % (OB < 32 ? OB : 32) == 0) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < NC; c0 += U) {
+            Raw<32> r[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) r[u] = ld_hint32(src + (c0 + u) * CH, pol_in);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                Out o[CH];
+#pragma unroll
+                for (int q = 0; q < CH; ++q) {
+                    acc = M::combine(acc, M::lift(convert<Acc>(raw_get<In>(r[u], q))));
+                    o[q] = convert<Out>(M::value(acc));
+                }
+                store_chunk<Out, CH>(dst + (c0 + u) * CH, o, pol_out);
+            }
+        }
+        return;
+    }
+    for (int i = 0; i < n; ++i) {
+        acc = M::combine(acc, M::lift(convert<Acc>(src[i])));
+        dst[i] = convert<Out>(M::value(acc));
+    }
+}
+
+// Lines that span several super-tiles of BLOCK x SEG elements. A persistent
+// block repeats: claim the next super-tile k; phase A of k -- every thread
+// streams its segment from HBM with an L2 evict-last hint and folds it, the
+// block keeps the segment totals in shared memory, reduces them in order
+// and publishes the super-tile's aggregate (for a line's first super-tile,
+// its inclusive prefix); then phase B of the super-tile it claimed one round
+// earlier -- look back to its exclusive prefix, publish its inclusive
+// prefix, scan the kept segment totals across the block, and every thread
+// walks its segment again (now from L2) from its own exclusive prefix,
+// storing as it goes. Phase A never waits, so every claimed super-tile's
+// aggregate appears promptly, and by the time a block looks back its
+// predecessors have long published: the waiting that a one-pass tile scan
+// does with the tile held in shared memory is done here with the data
+// parked in the 129 MB L2. HBM traffic stays one read and one write per
+// element; the operator is applied twice per element.
+template <class In, class Acc, class Out, class M, int BLOCK, int SEG>
+__global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Acc)>())
     k_scan_tiles(const In* __restrict__ x, Out* __restrict__ y, int64_t len, int64_t tiles_per_line, int64_t ntiles,
                  TileState<typename M::P> ts, ScanCtl ctl, bool has_init, Acc init) {
     using P = typename M::P;
-    using L = RunLayout<Acc, ITEMS>;
-    constexpr bool kPrefetch = std::is_same_v<In, Acc>;
-    extern __shared__ __align__(16) char smem_raw[];
-    const int B = blockDim.x;
-    const int W = B / kWarp;
+    constexpr int W = BLOCK / kWarp;
+    constexpr int64_t SUPER = (int64_t)BLOCK * SEG;
+    __shared__ P seg_tot[2][BLOCK];  // segment totals of the two open super-tiles
+    __shared__ P warp_tot[W];
+    __shared__ P red[W];
+    __shared__ int ints[2 * kWarp + 1];
+    __shared__ P s_bc;
+    __shared__ int64_t s_k;
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
-    const size_t tile_bytes = (size_t)B * L::stride * 16;
-    // buffer k of the (one or two) run tiles
-    auto buf_of = [&](int k) { return smem_raw + (kPrefetch ? (size_t)k * tile_bytes : 0); };
-    P* warp_tot = reinterpret_cast<P*>(smem_raw + (kPrefetch ? 2 : 1) * tile_bytes);
-    P* red = warp_tot + kWarp;
-    P* bcast = red + kWarp;  // [0] tile aggregate, [1] tile prefix
-    int* ints = reinterpret_cast<int*>(bcast + 2);  // [0..W) look-back scratch, [kWarp] stop flag
+    const uint64_t keep = l2_policy_evict_last();
+    const uint64_t last_use = l2_policy_evict_first();
 
-    const int tile_elems = B * ITEMS;
-    constexpr int VIN = sizeof(In) < 16 ? 16 / (int)sizeof(In) : 1;   // input elements per 16-byte load
-    constexpr int VOUT = sizeof(Out) < 16 ? 16 / (int)sizeof(Out) : 1;
-    static_assert(ITEMS % VIN == 0 && ITEMS % VOUT == 0, "runs must hold whole vectors");
-
-    // Starts the asynchronous copy of tile gg into buf; false when gg does not
-    // exist or is ragged / unaligned (those are loaded synchronously).
-    auto prefetch = [&](int64_t gg, char* buf) -> bool {
-        if constexpr (!kPrefetch) {
-            return false;
-        } else {
-            if (gg >= ntiles) return false;
-            const int64_t t = gg % tiles_per_line;
-            if (len - t * (int64_t)tile_elems < tile_elems) return false;
-            const In* src = x + (gg / tiles_per_line) * len + t * tile_elems;
-            if (reinterpret_cast<uintptr_t>(src) % 16 != 0) return false;
-            for (int v = tid; v < tile_elems / VIN; v += B) cp_async16(buf + L::elem_off(v * VIN), src + (int64_t)v * VIN);
-            return true;
-        }
-    };
-
-    int cur = 0;
-    bool have = prefetch(blockIdx.x, buf_of(0));
-    if constexpr (kPrefetch) cp_async_commit();
-
-    for (int64_t g = blockIdx.x; g < ntiles; g += gridDim.x) {
-        const int64_t line = g / tiles_per_line, t = g % tiles_per_line;
-        const int64_t start = line * len + t * tile_elems;
-        const int cnt = (int)min((int64_t)tile_elems, len - t * (int64_t)tile_elems);
-        const In* src = x + start;
-        Out* dst = y + start;
-        char* tile = buf_of(cur);
-
-        bool have_next = false;
-        if constexpr (kPrefetch) {
-            have_next = prefetch(g + gridDim.x, buf_of(cur ^ 1));
-            cp_async_commit();
-            cp_async_wait<1>();  // this tile's group has landed (the newest may still fly)
-        }
-        // ---- striped load into the padded run layout (when not prefetched)
-        if (!have) {
-            const bool vec_in = cnt == tile_elems && (reinterpret_cast<uintptr_t>(src) % 16 == 0);
-            if (vec_in) {
-                for (int v = tid; v < tile_elems / VIN; v += B) {
-                    In e[VIN];
-                    if constexpr (VIN > 1) {
-                        Raw<16> r = ld_stream16(src + (int64_t)v * VIN);
-                        memcpy(e, &r, 16);
-                    } else {
-                        e[0] = src[v];
-                    }
-                    Acc a[VIN];
-#pragma unroll
-                    for (int q = 0; q < VIN; ++q) a[q] = convert<Acc>(e[q]);
-                    smem_store(tile + L::elem_off(v * VIN), a);
-                }
-            } else {
-                for (int e = tid; e < tile_elems; e += B) {
-                    Acc a;
-                    if (e < cnt) a = convert<Acc>(src[e]);
-                    else memset(&a, 0, sizeof a);
-                    *reinterpret_cast<Acc*>(tile + L::elem_off(e)) = a;
+    int64_t prev = -1;
+    P prev_agg = M::empty();
+    int slot = 0;
+    while (true) {
+        if (tid == 0) s_k = claim_tile(ctl, ntiles);
+        __syncthreads();
+        const int64_t k = s_k;
+        P agg = M::empty();
+        if (k < ntiles) {
+            // ---- phase A of super-tile k
+            const int64_t t = k % tiles_per_line;
+            const int64_t start = (k / tiles_per_line) * len + t * SUPER;
+            const int64_t cnt = min(SUPER, len - t * SUPER);
+            const int n = (int)max((int64_t)0, min((int64_t)SEG, cnt - (int64_t)tid * SEG));
+            const P tot = n > 0 ? segment_fold<In, M, SEG>(x + start + (int64_t)tid * SEG, n, keep) : M::empty();
+            seg_tot[slot][tid] = tot;
+            if (tiles_per_line > 1) {
+                agg = block_reduce_ordered<M, BLOCK>(tot, red);
+                const bool last = (t == tiles_per_line - 1);
+                if (tid == 0 && !last && k != ctl.skip_tile) {
+                    if (t == 0) publish(ts, k, kStatusPrefix, M::combine(has_init ? M::lift(init) : M::empty(), agg), ctl.epoch);
+                    else publish(ts, k, kStatusAggregate, agg, ctl.epoch);
                 }
             }
         }
-        __syncthreads();
-
-        // ---- each thread scans its run in registers
-        Acc run[ITEMS];
-        smem_load(run, L::run_ptr(tile, tid));
-#pragma unroll
-        for (int i = 1; i < ITEMS; ++i) run[i] = M::op::apply(run[i - 1], run[i]);
-        // elements past the end of a ragged tile must not reach the aggregate
-        const int valid_items = min(ITEMS, max(0, cnt - tid * ITEMS));
-        P total = M::lift(run[ITEMS - 1]);
-        if (valid_items < ITEMS) {
-            // ragged run: predicated fold of the valid elements (still in smem)
-            Acc orig[ITEMS];
-            smem_load(orig, L::run_ptr(tile, tid));
-            total = M::empty();
-#pragma unroll
-            for (int i = 0; i < ITEMS; ++i)
-                if (i < valid_items) total = M::combine(total, M::lift(orig[i]));
-        }
-
-        // ---- block scan of run totals (thread order)
-        P inc = warp_inclusive_scan<M>(total, lane);
-        P lane_excl = shfl_up_any(inc, 1);
-        if (lane == 0) lane_excl = M::empty();
-        if (lane == kWarp - 1) warp_tot[warp] = inc;
-        __syncthreads();
-        if (warp == 0) {
-            P w = lane < W ? warp_tot[lane] : M::empty();
-            P wi = warp_inclusive_scan<M>(w, lane);
-            P we = shfl_up_any(wi, 1);
-            if (lane == 0) we = M::empty();
-            if (lane < W) warp_tot[lane] = we;  // exclusive base of each warp
-            if (lane == 0) bcast[0] = shfl_idx_any(wi, W - 1);
-            else shfl_idx_any(wi, W - 1);
-        }
-        __syncthreads();
-
-        // ---- tile prefix: publish the aggregate, look back, publish the prefix
-        const P agg = bcast[0];
-        const bool first = (t == 0);
-        const bool last = (t == tiles_per_line - 1);
-        const bool skip = (g == ctl.skip_tile);
-        P prefix = M::empty();
-        if (first) {
-            if (has_init) prefix = M::lift(init);
-            if (tid == 0 && !last && !skip) publish(ts, g, kStatusPrefix, M::combine(prefix, agg), ctl.epoch);
-        } else {
-            if (tid == 0 && !last && !skip) publish(ts, g, kStatusAggregate, agg, ctl.epoch);
-            if (!block_look_back<M>(g, g - t, ts, ctl, red, ints, &prefix)) {
-                if (tid == 0)
-                    atomicExch(reinterpret_cast<unsigned long long*>(ctl.error_word), (unsigned long long)ctl.epoch);
-                if constexpr (kPrefetch) cp_async_wait<0>();  // no copy may outlive the block
-                return;  // uniform: every thread got the same answer
-            }
-            if (tid == 0 && !last && !skip) publish(ts, g, kStatusPrefix, M::combine(prefix, agg), ctl.epoch);
-        }
-        if (tid == 0) bcast[1] = prefix;
-        __syncthreads();
-
-        // ---- apply prefixes to the run, write back
-        const P base = M::combine(M::combine(bcast[1], warp_tot[warp]), lane_excl);
-#pragma unroll
-        for (int i = 0; i < ITEMS; ++i) run[i] = M::value(M::combine(base, M::lift(run[i])));
-        smem_store(L::run_ptr(tile, tid), run);
-        __syncthreads();
-
-        // ---- striped store
-        const bool vec_out = cnt == tile_elems && (reinterpret_cast<uintptr_t>(dst) % 16 == 0);
-        if (vec_out) {
-            for (int v = tid; v < tile_elems / VOUT; v += B) {
-                Acc a[VOUT];
-                smem_load(a, tile + L::elem_off(v * VOUT));
-                Out o[VOUT];
-#pragma unroll
-                for (int q = 0; q < VOUT; ++q) o[q] = convert<Out>(a[q]);
-                if constexpr (VOUT > 1) {
-                    Raw<16> r;
-                    memcpy(&r, o, 16);
-                    st_global16(dst + (int64_t)v * VOUT, r);
-                } else {
-                    dst[v] = o[0];
+        if (prev >= 0) {
+            // ---- phase B of super-tile prev
+            const int pslot = slot ^ 1;
+            const int64_t t = prev % tiles_per_line;
+            const int64_t start = (prev / tiles_per_line) * len + t * SUPER;
+            const int64_t cnt = min(SUPER, len - t * SUPER);
+            P prefix = has_init ? M::lift(init) : M::empty();
+            if (t != 0) {
+                if (!look_back<M, BLOCK>(prev, prev - t, ts, ctl, red, ints, &prefix)) {
+                    if (tid == 0)
+                        atomicExch(reinterpret_cast<unsigned long long*>(ctl.error_word), (unsigned long long)ctl.epoch);
+                    return;  // uniform: every thread got the same answer
                 }
+                if (tid == 0 && t != tiles_per_line - 1 && prev != ctl.skip_tile)
+                    publish(ts, prev, kStatusPrefix, M::combine(prefix, prev_agg), ctl.epoch);
+                if (tid == 0) s_bc = prefix;
+                __syncthreads();
+                prefix = s_bc;
             }
-        } else {
-            for (int e = tid; e < cnt; e += B) {
-                dst[e] = convert<Out>(*reinterpret_cast<const Acc*>(tile + L::elem_off(e)));
+            // exclusive prefix of this thread's segment: prefix + earlier segments
+            const P tot = seg_tot[pslot][tid];
+            const P inc = warp_inclusive_scan<M>(tot, lane);
+            P lane_excl = shfl_up_any(inc, 1);
+            if (lane == 0) lane_excl = M::empty();
+            if (lane == kWarp - 1) warp_tot[warp] = inc;
+            __syncthreads();
+            if (warp == 0) {
+                const P w = lane < W ? warp_tot[lane] : M::empty();
+                const P wi = warp_inclusive_scan<M>(w, lane);
+                P we = shfl_up_any(wi, 1);
+                if (lane == 0) we = M::empty();
+                if (lane < W) warp_tot[lane] = we;
             }
+            __syncthreads();
+            const P mine = M::combine(M::combine(prefix, warp_tot[warp]), lane_excl);
+            const int n = (int)max((int64_t)0, min((int64_t)SEG, cnt - (int64_t)tid * SEG));
+            if (n > 0)
+                segment_scan_store<In, Out, M, SEG>(x + start + (int64_t)tid * SEG, y + start + (int64_t)tid * SEG, n,
+                                                    mine, last_use, last_use);
+            __syncthreads();  // warp_tot and the slot are reused next
         }
-        __syncthreads();  // this buffer is refilled two tiles later
-        have = have_next;
-        cur ^= 1;
+        if (k >= ntiles) break;
+        prev = k;
+        prev_agg = agg;
+        slot ^= 1;
     }
-    if constexpr (kPrefetch) cp_async_wait<0>();
+}
+
+// Lines that fit one tile: block b scans line b with the init prefix; no
+// state is shared between blocks.
+template <class In, class Acc, class Out, class M, int ITEMS, int BLOCK>
+__global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Acc)>())
+    k_scan_lines(const In* __restrict__ x, Out* __restrict__ y, int64_t len, bool has_init, Acc init) {
+    using P = typename M::P;
+    using L = RunLayout<Acc, ITEMS>;
+    constexpr int W = BLOCK / kWarp;
+    __shared__ __align__(16) char tile[BLOCK * L::stride * 16];
+    __shared__ P warp_tot[W];
+    __shared__ P s_prefix;
+    const int64_t start = (int64_t)blockIdx.x * len;
+    const int cnt = (int)len;
+    if (threadIdx.x == 0) s_prefix = has_init ? M::lift(init) : M::empty();
+    load_tile<In, Acc, ITEMS, BLOCK>(tile, x + start, cnt, l2_policy_evict_first());
+    __syncthreads();
+    scan_apply_store<Acc, Out, M, ITEMS, BLOCK>(tile, y + start, cnt, &s_prefix, warp_tot, l2_policy_evict_first());
 }
 
 // Lines along a strided dimension: y[i + I*(j + J*k)] over j, for every
@@ -419,13 +740,6 @@ __global__ void __launch_bounds__(256) k_scan_strided(const In* __restrict__ x, 
     }
 }
 
-template <class In, class Acc, class M>
-size_t tile_smem_bytes(int block) {
-    using L = RunLayout<Acc, default_items<Acc>()>;
-    const size_t bufs = std::is_same_v<In, Acc> ? 2 : 1;
-    return bufs * block * L::stride * 16 + (2 * kWarp + 2) * sizeof(typename M::P) + (kWarp + 4) * sizeof(int);
-}
-
 template <class In, class Acc, class Out, class M>
 ak_status launch(const ScanCall& c, const ScanPlan& p) {
     using P = typename M::P;
@@ -441,42 +755,48 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
         return s;
     }
     constexpr int ITEMS = default_items<Acc>();
+    constexpr int BLOCK = default_block<Acc>();
+    constexpr int SEG = default_seg<Acc>();
     if constexpr (!(ITEMS % (sizeof(In) < 16 ? 16 / sizeof(In) : 1) == 0 &&
                     ITEMS % (sizeof(Out) < 16 ? 16 / sizeof(Out) : 1) == 0)) {
         return AK_ERR_UNSUPPORTED;
     } else {
-        auto kernel = k_scan_tiles<In, Acc, Out, M, ITEMS>;
-        const size_t smem = tile_smem_bytes<In, Acc, M>(p.block);
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return cuda_fail(e);
-        int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, p.block, smem);
-        if (e != cudaSuccess) return cuda_fail(e);
-        DeviceInfo dev;
-        if (!current_device(&dev)) return AK_ERR_CUDA;
-        int64_t grid = std::min<int64_t>(p.tiles, (int64_t)std::max(occ, 1) * dev.sm_count);
-        if (c.target_blocks > 0) grid = std::min<int64_t>(grid, c.target_blocks);
+        if (p.block != BLOCK || p.items != ITEMS) return AK_ERR_UNSUPPORTED;
         char* ws = static_cast<char*>(c.ws);
         TileState<P> ts;
-        ts.flags = reinterpret_cast<uint64_t*>(ws + p.state_off);
-        ts.aggs = reinterpret_cast<P*>(ws + p.state_off + align_up((size_t)p.tiles * 8, 16));
-        ts.incls = ts.aggs + p.tiles;
+        ts.recs = reinterpret_cast<TileRec<P>*>(ws + p.state_off);
         ScanCtl ctl;
         ctl.epoch = c.epoch;
         ctl.error_word = reinterpret_cast<uint64_t*>(ws);  // WsHeader::error_word
+        ctl.counter = reinterpret_cast<unsigned long long*>(ws + 64);
         ctl.wait_limit_ns = c.wait_limit_ns;
         ctl.skip_tile = c.skip_tile;
-        const In* xs = static_cast<const In*>(c.src);
-        Out* ys = static_cast<Out*>(c.dst);
-        int64_t len = c.len, tpl = p.tiles_per_line, nt = p.tiles;
-        bool hi = c.has_init;
-        void* args[] = {(void*)&xs, (void*)&ys, (void*)&len, (void*)&tpl, (void*)&nt, (void*)&ts,
-                        (void*)&ctl, (void*)&hi, (void*)&init};
-        e = cudaLaunchCooperativeKernel((const void*)kernel, dim3((unsigned)grid), dim3(p.block), args, smem,
-                                        c.stream);
-        if (e != cudaSuccess) return cuda_fail(e);
-        count_launches(1);
-        return AK_OK;
+        if (p.kind == 2) {
+            // the smallest block whose tile holds a whole line
+            auto lines = [&](auto blk) {
+                constexpr int B = decltype(blk)::value;
+                k_scan_lines<In, Acc, Out, M, ITEMS, B><<<(unsigned)p.tiles, B, 0, c.stream>>>(
+                    static_cast<const In*>(c.src), static_cast<Out*>(c.dst), c.len, c.has_init, init);
+            };
+            if (c.len <= 64 * ITEMS) lines(std::integral_constant<int, 64>{});
+            else if (c.len <= 128 * ITEMS || BLOCK == 128) lines(std::integral_constant<int, 128>{});
+            else lines(std::integral_constant<int, BLOCK>{});
+        } else {
+            DeviceInfo dev;
+            if (!current_device(&dev)) return AK_ERR_CUDA;
+            int occ = 0;
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &occ, k_scan_tiles<In, Acc, Out, M, BLOCK, SEG>, BLOCK, 0);
+            if (e != cudaSuccess) return cuda_fail(e);
+            int64_t grid = std::min<int64_t>(p.tiles, (int64_t)std::max(occ, 1) * dev.sm_count);
+            if (c.target_blocks > 0) grid = std::min<int64_t>(grid, c.target_blocks);
+            k_scan_tiles<In, Acc, Out, M, BLOCK, SEG><<<(unsigned)grid, BLOCK, 0, c.stream>>>(
+                static_cast<const In*>(c.src), static_cast<Out*>(c.dst), c.len, p.tiles_per_line, p.tiles, ts, ctl,
+                c.has_init, init);
+        }
+        ak_status s = check_launch();
+        if (s == AK_OK) count_launches(1);
+        return s;
     }
 }
 
@@ -502,22 +822,23 @@ ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_d
         return AK_OK;
     }
     p->kind = 0;
-    const int it = asz >= 16 ? 8 : (asz == 8 ? 8 : 16);
+    const int it = asz >= 16 ? 8 : (asz == 8 ? 16 : 32);
     if (items != 0 && items != it) return AK_ERR_UNSUPPORTED;
     p->items = it;
-    // Block size: the smallest of 128 / 256 / 512 threads whose tile holds a
-    // whole line, else 512 (fewer, larger tiles for long lines).
-    const int max_block = asz >= 16 ? 256 : kMaxBlock;
-    int block = max_block;
-    for (int b : {128, 256, 512}) {
-        if (b <= max_block && (int64_t)b * it >= len) { block = b; break; }
-    }
+    const int block = asz >= 16 ? 128 : 256;
+    const int seg = asz >= 16 ? 64 : (asz == 8 ? 64 : 128);
     p->block = block;
     const int64_t tile = (int64_t)block * it;
-    p->tiles_per_line = (len + tile - 1) / tile;
+    if (len <= tile) {
+        p->kind = 2;  // every line fits one tile: no state shared between blocks
+        p->tiles_per_line = 1;
+        p->tiles = outer;
+        return AK_OK;
+    }
+    const int64_t super = (int64_t)block * seg;
+    p->tiles_per_line = (len + super - 1) / super;
     p->tiles = p->tiles_per_line * outer;
-    if (p->tiles_per_line > 1)
-        p->ws_bytes = align_up(kWsHeader + align_up((size_t)p->tiles * 8, 16) + 2 * (size_t)p->tiles * psz, 256);
+    p->ws_bytes = align_up(kWsHeader + (size_t)p->tiles * (16 + align_up(psz, 16)), 256);  // TileRec per super-tile
     return AK_OK;
 }
 
