@@ -97,11 +97,12 @@ def test_accumulate_validates_and_plans_on_host(L):
     assert acc(dst=0x1000 + 64) == INV        # partial overlap
     assert acc(in_t=5, a=5, o=5, op=0) == UNS
     b = ctypes.c_size_t()
-    # whole-array f64 scan of 1e8: 512 x 8 tiles, one state word + two partials each
+    # whole-array f64 scan of 1e8: super-tiles of 256 threads x 64 elements,
+    # one 32-byte state record each (tag, check word, value)
     n = (ctypes.c_int64 * 1)(10**8)
     assert L.ak_accumulate_workspace_size(1, n, -1, 1, 1, 0, None, ctypes.byref(b)) == 0
-    tiles = -(-10**8 // 4096)
-    assert b.value >= 256 + tiles * (8 + 16)
+    tiles = -(-10**8 // (256 * 64))
+    assert b.value >= 256 + tiles * 32
     # columns of 4096 f32 fit one tile each: no tile state needed
     assert L.ak_accumulate_workspace_size(2, sh, 0, 0, 0, 0, None, ctypes.byref(b)) == 0
     assert b.value == 256
