@@ -183,7 +183,8 @@ struct DimsPlan {
     int vec;          // elements per vector load along the contiguous dimension
     int tile_out;     // outputs per block along the contiguous dimension
     int row_groups;   // reduction rows processed in parallel per block
-    int split;        // blocks along the reduction (> 1: second pass)
+    int split;        // blocks along the reduction (> 1: combined in a cluster or by a second pass)
+    bool cluster;     // the split blocks of an output tile form one thread-block cluster
     size_t ws_bytes;
 };
 ak_status plan_dims(const DimsCall& c, const DeviceInfo& dev, DimsPlan* plan);

@@ -19,6 +19,9 @@ namespace {
 
 using dims::kBlock;
 using dims::kMinRowsPerGroup;
+constexpr int kMaxCluster = 16;
+// fewest reduction rows a block of a cluster should get
+constexpr int64_t R_rows_min(int row_groups) { return (int64_t)row_groups * 2; }
 
 template <class Out>
 __global__ void k_fill(Out* dst, int64_t count, Out v) {
@@ -33,9 +36,8 @@ __global__ void k_fill(Out* dst, int64_t count, Out v) {
 // threads with vec-wide loads. The reduction is split only as far as needed
 // to give the device about target_ctas blocks, and never below
 // kMinRowsPerGroup rows per group.
-static void select_shape(int64_t I, int64_t J, int64_t K, int vec, int sm_count, int forced,
+static void select_shape(int64_t I, int64_t J, int64_t K, int esz, int vec, int sm_count, int forced,
                          DimsPlan* p) {
-    const int64_t target_ctas = (int64_t)sm_count * (2048 / kBlock);
     const int64_t vecs_per_row = (I + vec - 1) / vec;
     // Enough outputs that one thread per vector of outputs already puts
     // kUnroll loads in flight on every thread slot of the device.
@@ -43,6 +45,7 @@ static void select_shape(int64_t I, int64_t J, int64_t K, int vec, int sm_count,
     int shape = forced;
     if (shape == AK_SHAPE_AUTO) shape = (J < 32 || many_outputs) ? AK_SHAPE_THREAD : AK_SHAPE_COLUMNS;
     p->vec = vec;
+    p->cluster = false;
     if (shape == AK_SHAPE_THREAD) {
         const int tpr = (int)std::min<int64_t>(kBlock, vecs_per_row);
         p->tile_out = tpr * vec;
@@ -51,11 +54,45 @@ static void select_shape(int64_t I, int64_t J, int64_t K, int vec, int sm_count,
         p->shape = AK_SHAPE_THREAD;
         return;
     }
-    const int tpr = (int)std::min<int64_t>(32, vecs_per_row);
-    p->tile_out = tpr * vec;
-    p->row_groups = kBlock / tpr;
-    const int64_t col_tiles = ((I + p->tile_out - 1) / p->tile_out) * K;
-    int64_t split = (target_ctas + col_tiles - 1) / col_tiles;
+    // Blocks wanted: enough that one round of kUnroll 16-byte loads per thread
+    // covers the whole input (latency-bound sizes), at most 8 per SM.
+    const int64_t bytes = I * J * K * esz;
+    const int64_t per_block = (int64_t)kBlock * dims::kUnroll * 16;
+    const int64_t target = std::max<int64_t>(sm_count, std::min<int64_t>((int64_t)sm_count * 8,
+                                                                         (bytes + per_block - 1) / per_block));
+    auto set_tile = [&](int tpr) {
+        p->tile_out = tpr * vec;
+        p->row_groups = kBlock / tpr;
+        return ((I + p->tile_out - 1) / p->tile_out) * K;  // output tiles
+    };
+    if (shape == AK_SHAPE_COLUMNS) {
+        // Prefer a cluster split (2..16 blocks per output tile, partials
+        // combined in distributed shared memory): try row segments of 32,
+        // 16, 8 and 4 threads until the wanted split fits a cluster.
+        for (int tpr : {32, 16, 8, 4}) {
+            if (tpr > vecs_per_row && tpr != 4) continue;
+            const int64_t tiles = set_tile((int)std::min<int64_t>(tpr, vecs_per_row));
+            const int64_t want = (target + tiles - 1) / tiles;
+            if (want <= 1) {
+                p->split = 1;
+                p->shape = AK_SHAPE_TILED;
+                return;
+            }
+            if (want <= kMaxCluster) {
+                int cs = 2;
+                while (cs < want) cs *= 2;
+                if ((int64_t)cs * R_rows_min(p->row_groups) <= J) {
+                    p->split = cs;
+                    p->cluster = true;
+                    p->shape = AK_SHAPE_COLUMNS;
+                    return;
+                }
+            }
+        }
+    }
+    // Split through a workspace and a second pass (or no split: tiled).
+    const int64_t tiles = set_tile((int)std::min<int64_t>(32, vecs_per_row));
+    int64_t split = (target + tiles - 1) / tiles;
     const int64_t max_split = std::max<int64_t>(1, J / ((int64_t)p->row_groups * kMinRowsPerGroup));
     split = std::max<int64_t>(1, std::min<int64_t>(split, max_split));
     split = std::min<int64_t>(split, 65535);
@@ -71,6 +108,7 @@ ak_status plan_dims(const DimsCall& c, const DeviceInfo& dev, DimsPlan* p) {
     if (!psz || !esz) return AK_ERR_UNSUPPORTED;
     p->ws_bytes = kWsHeader;
     p->split = 1;
+    p->cluster = false;
     p->vec = 1;
     p->tile_out = 1;
     p->row_groups = 1;
@@ -87,9 +125,10 @@ ak_status plan_dims(const DimsCall& c, const DeviceInfo& dev, DimsPlan* p) {
         const uintptr_t addr = reinterpret_cast<uintptr_t>(c.src);
         int vec = 1;
         if (esz < 16 && addr % 16 == 0 && (c.inner * (int64_t)esz) % 16 == 0) vec = (int)(16 / esz);
-        select_shape(c.inner, c.red, c.outer, vec, dev.sm_count, c.forced_shape, p);
+        select_shape(c.inner, c.red, c.outer, (int)esz, vec, dev.sm_count, c.forced_shape, p);
     }
-    if (p->split > 1) p->ws_bytes = align_up(kWsHeader + (size_t)p->split * c.inner * c.outer * psz, 256);
+    if (p->split > 1 && !p->cluster)
+        p->ws_bytes = align_up(kWsHeader + (size_t)p->split * c.inner * c.outer * psz, 256);
     return AK_OK;
 }
 
@@ -129,7 +168,7 @@ extern "C" ak_status ak_dims_select(int64_t inner, int64_t red_len, int64_t oute
         forced_shape < AK_SHAPE_AUTO || forced_shape > AK_SHAPE_COLUMNS || vec_elems * elem_bytes > 16)
         return AK_ERR_INVALID_ARG;
     ak::DimsPlan p = {};
-    ak::select_shape(inner, red_len, outer, vec_elems, sm_count, forced_shape, &p);
+    ak::select_shape(inner, red_len, outer, elem_bytes, vec_elems, sm_count, forced_shape, &p);
     if (shape_out) *shape_out = p.shape;
     if (tile_outputs) *tile_outputs = p.tile_out;
     if (row_groups) *row_groups = p.row_groups;

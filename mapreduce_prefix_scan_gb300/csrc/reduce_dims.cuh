@@ -27,6 +27,7 @@
 // "tiled" = several groups, no split, "columns" = several groups and a split.
 #pragma once
 #include <algorithm>
+#include <cooperative_groups.h>
 
 #include "ak_common.cuh"
 #include "ak_internal.h"
@@ -73,7 +74,14 @@ __device__ __forceinline__ void load_row(const In* p, In (&r)[VB / sizeof(In)]) 
 }
 
 // VB = bytes per load: 16 (vector of 16/sizeof(In) outputs) or sizeof(In).
-template <class In, class Acc, class Out, class Map, class M, int VB>
+// CLUSTER: the `split` blocks of one output tile form a thread-block
+// cluster (split = cluster size); each keeps its partial outputs in shared
+// memory and, after a cluster barrier, rank r folds the partials of its
+// share of the outputs from every rank's shared memory (distributed shared
+// memory), in rank (= row) order, and stores them: no workspace, no second
+// pass. Otherwise blockIdx.y is the split index and split > 1 writes
+// partials for k_dims_finish.
+template <class In, class Acc, class Out, class Map, class M, int VB, bool CLUSTER>
 __global__ void __launch_bounds__(kBlock) k_dims_strided(const In* __restrict__ x, int64_t I, int64_t J,
                                                          int64_t K, int tile_out, int tpr, int R,
                                                          int split, typename M::P* __restrict__ partials,
@@ -83,8 +91,9 @@ __global__ void __launch_bounds__(kBlock) k_dims_strided(const In* __restrict__ 
     __shared__ P smem[kBlock * V];
 
     const int64_t tiles_i = (I + tile_out - 1) / tile_out;
-    const int64_t ct = blockIdx.x % tiles_i, k = blockIdx.x / tiles_i;
-    const int s = blockIdx.y;
+    const int64_t tile_id = CLUSTER ? blockIdx.x / split : blockIdx.x;
+    const int64_t ct = tile_id % tiles_i, k = tile_id / tiles_i;
+    const int s = CLUSTER ? (int)(blockIdx.x % split) : (int)blockIdx.y;
     const int tid = threadIdx.x, c = tid % tpr, rg = tid / tpr;
     const int64_t i0 = ct * tile_out + (int64_t)c * V;
 
@@ -133,13 +142,42 @@ __global__ void __launch_bounds__(kBlock) k_dims_strided(const In* __restrict__ 
         for (int q = 0; q < V; ++q) smem[rg * tile_out + c * V + q] = acc[q];
     }
     __syncthreads();
-    for (int o = tid; o < tile_out; o += kBlock) {
-        const int64_t i = ct * tile_out + o;
-        if (i >= I) continue;
-        P a = smem[o];
-        for (int g = 1; g < R; ++g) a = M::combine(a, smem[g * tile_out + o]);
-        if (split == 1) dims_store<Acc, Out, M>(a, st, i + I * k);
-        else partials[((int64_t)s * K + k) * I + i] = a;
+    if constexpr (CLUSTER) {
+        // this block's partial outputs go to the front of smem (row groups
+        // combined in order), then the cluster folds them rank by rank
+        namespace cg = cooperative_groups;
+        cg::cluster_group cluster = cg::this_cluster();
+        P part[(kBlock * V + kBlock - 1) / kBlock];
+        int np = 0;
+        for (int o = tid; o < tile_out; o += kBlock, ++np) {
+            P a = smem[o];
+            for (int g = 1; g < R; ++g) a = M::combine(a, smem[g * tile_out + o]);
+            part[np] = a;
+        }
+        __syncthreads();
+        np = 0;
+        for (int o = tid; o < tile_out; o += kBlock, ++np) smem[o] = part[np];
+        cluster.sync();
+        const int per = (tile_out + split - 1) / split;
+        const int o = s * per + tid;
+        if (tid < per && o < tile_out) {
+            const int64_t i = ct * tile_out + o;
+            if (i < I) {
+                P a = *cluster.map_shared_rank(smem + o, 0);
+                for (int q = 1; q < split; ++q) a = M::combine(a, *cluster.map_shared_rank(smem + o, q));
+                dims_store<Acc, Out, M>(a, st, i + I * k);
+            }
+        }
+        cluster.sync();  // no block leaves while others read its shared memory
+    } else {
+        for (int o = tid; o < tile_out; o += kBlock) {
+            const int64_t i = ct * tile_out + o;
+            if (i >= I) continue;
+            P a = smem[o];
+            for (int g = 1; g < R; ++g) a = M::combine(a, smem[g * tile_out + o]);
+            if (split == 1) dims_store<Acc, Out, M>(a, st, i + I * k);
+            else partials[((int64_t)s * K + k) * I + i] = a;
+        }
     }
 }
 
@@ -196,7 +234,15 @@ __global__ void __launch_bounds__(kBlock) k_dims_finish(const typename M::P* par
     const int64_t o = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     if (o >= nout) return;
     typename M::P a = partials[o];
-    for (int s = 1; s < split; ++s) a = M::combine(a, partials[(int64_t)s * nout + o]);
+    int s = 1;
+    for (; s + 8 <= split; s += 8) {  // 8 loads in flight, folded in split order
+        typename M::P v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = partials[(int64_t)(s + u) * nout + o];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) a = M::combine(a, v[u]);
+    }
+    for (; s < split; ++s) a = M::combine(a, partials[(int64_t)s * nout + o]);
     dims_store<Acc, Out, M>(a, st, o);
 }
 
@@ -285,20 +331,45 @@ ak_status launch(const DimsCall& c, const DimsPlan& p) {
     } else {
         const int64_t tiles_i = (c.inner + p.tile_out - 1) / p.tile_out;
         const int tpr = p.tile_out / p.vec;
-        dim3 grid((unsigned)(tiles_i * c.outer), (unsigned)p.split);
-        if (p.vec > 1) {
-            if constexpr (16 % sizeof(In) == 0 && sizeof(In) < 16)
-                k_dims_strided<In, Acc, Out, Map, M, 16><<<grid, kBlock, 0, c.stream>>>(
-                    x, c.inner, c.red, c.outer, p.tile_out, tpr, p.row_groups, p.split, partials, st);
-        } else {
-            k_dims_strided<In, Acc, Out, Map, M, (int)sizeof(In)><<<grid, kBlock, 0, c.stream>>>(
+        auto go = [&](auto vb) -> cudaError_t {
+            constexpr int VB = decltype(vb)::value;
+            if (p.cluster) {
+                auto kernel = k_dims_strided<In, Acc, Out, Map, M, VB, true>;
+                if (p.split > 8) {
+                    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                    if (e != cudaSuccess) return e;
+                }
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3((unsigned)(tiles_i * c.outer * p.split));
+                cfg.blockDim = dim3(kBlock);
+                cfg.stream = c.stream;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = (unsigned)p.split;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                return cudaLaunchKernelEx(&cfg, kernel, x, c.inner, c.red, c.outer, p.tile_out, tpr, p.row_groups,
+                                          p.split, partials, st);
+            }
+            dim3 grid((unsigned)(tiles_i * c.outer), (unsigned)p.split);
+            k_dims_strided<In, Acc, Out, Map, M, VB, false><<<grid, kBlock, 0, c.stream>>>(
                 x, c.inner, c.red, c.outer, p.tile_out, tpr, p.row_groups, p.split, partials, st);
+            return cudaGetLastError();
+        };
+        cudaError_t e = cudaSuccess;
+        if (p.vec > 1) {
+            if constexpr (16 % sizeof(In) == 0 && sizeof(In) < 16) e = go(std::integral_constant<int, 16>{});
+        } else {
+            e = go(std::integral_constant<int, (int)sizeof(In)>{});
         }
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     ak_status s = check_launch();
     if (s != AK_OK) return s;
     count_launches(1);
-    if (p.split > 1) {
+    if (p.split > 1 && !p.cluster) {
         dim3 grid((unsigned)((nout + kBlock - 1) / kBlock));
         cudaError_t e = launch_finish<Acc, Out, M>(grid, c.stream, (const P*)partials, nout, p.split, st);
         if (e != cudaSuccess) return cuda_fail(e);

@@ -24,12 +24,12 @@
 // tiles' loads. A block takes its tile index from an atomic counter when it
 // starts, so every tile it waits for belongs to a block that is already
 // running: progress never depends on the order in which the hardware
-// dispatches blocks. The counter and every tile-state word carry the call's
-// epoch, so stale state from earlier calls is never mistaken for current
-// state and the workspace needs no clearing. Every wait is bounded by a
-// global-timer deadline; a block that gives up records the epoch in the
-// workspace's error word, which every other waiter also watches, and all
-// blocks leave early.
+// dispatches blocks. Each call clears the counter and the tile records on its
+// own stream before the kernel (so a call captured in a CUDA graph is correct
+// on every replay), and every record also carries the call's epoch. Every
+// wait is bounded by a global-timer deadline; a block that gives up records
+// the epoch in the workspace's error word, which every other waiter also
+// watches, and all blocks leave early.
 #include <algorithm>
 
 #include "ak_common.cuh"
@@ -179,7 +179,7 @@ __device__ __forceinline__ uint64_t read_rec(const TileRec<P>* r, uint64_t epoch
 struct ScanCtl {
     uint64_t epoch;
     uint64_t* error_word;
-    unsigned long long* counter;  // tile claims: [0] tag (epoch << 1 | ready), [1] next index
+    unsigned long long* counter;  // next tile index (zeroed by the call before the kernel)
     int64_t wait_limit_ns;
     int64_t skip_tile;  // fault injection; -1 = off
 };
@@ -188,33 +188,12 @@ __device__ __forceinline__ bool aborted(const ScanCtl& ctl) {
     return ld_relaxed_u64(ctl.error_word) == ctl.epoch;
 }
 
-// The next tile index of this call. Two header words: `tag` says which call
-// owns the count and whether it has been reset, `count` hands out indices.
-// The first block of a call that sees a stale tag (an earlier call, or
-// uninitialised memory) wins a compare-and-swap to "resetting", zeroes the
-// count, and releases the tag as "ready"; every other block waits (bounded)
-// for "ready" and then takes an index with one atomic add. Returns ntiles
-// when the wait runs out (the block then does nothing).
+// The next tile index of this call: the call zeroes the counter on its
+// stream before the kernel (a memset node when the call is captured in a
+// CUDA graph), so claims are plain atomic adds in claim order.
 __device__ __forceinline__ int64_t claim_tile(const ScanCtl& ctl, int64_t ntiles) {
-    const unsigned long long resetting = (unsigned long long)ctl.epoch << 1;
-    const unsigned long long ready = resetting | 1ull;
-    unsigned long long* tag = ctl.counter;
-    unsigned long long* count = ctl.counter + 1;
-    // The winner's count reset is performed at L2 before its tag store is
-    // issued, so a block that sees "ready" and then adds at L2 sees the reset.
-    unsigned long long a = ld_relaxed_u64(reinterpret_cast<uint64_t*>(tag));
-    if (a == ready) return (int64_t)atomicAdd(count, 1ull);
-    if (a != resetting && atomicCAS(tag, a, resetting) == a) {
-        atomicExch(count, 1ull);  // index 0 is ours
-        st_relaxed_u64(reinterpret_cast<uint64_t*>(tag), ready);
-        return 0;
-    }
-    const uint64_t t_start = globaltimer_ns();
-    while (ld_relaxed_u64(reinterpret_cast<uint64_t*>(tag)) != ready) {
-        if (globaltimer_ns() - t_start > (uint64_t)ctl.wait_limit_ns) return ntiles;
-        __nanosleep(64);
-    }
-    return (int64_t)atomicAdd(count, 1ull);
+    (void)ntiles;
+    return (int64_t)atomicAdd(ctl.counter, 1ull);
 }
 
 // Ordered combine over the block (thread 0 leftmost); result in thread 0;
@@ -790,6 +769,12 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
             if (e != cudaSuccess) return cuda_fail(e);
             int64_t grid = std::min<int64_t>(p.tiles, (int64_t)std::max(occ, 1) * dev.sm_count);
             if (c.target_blocks > 0) grid = std::min<int64_t>(grid, c.target_blocks);
+            // Fresh claim counter, error word and tile records for this call. The
+            // records also carry the call's epoch; zeroing them makes a call
+            // captured in a CUDA graph (whose epoch is fixed at capture) correct
+            // on every replay.
+            e = cudaMemsetAsync(ws, 0, p.ws_bytes, c.stream);
+            if (e != cudaSuccess) return cuda_fail(e);
             k_scan_tiles<In, Acc, Out, M, BLOCK, SEG><<<(unsigned)grid, BLOCK, 0, c.stream>>>(
                 static_cast<const In*>(c.src), static_cast<Out*>(c.dst), c.len, p.tiles_per_line, p.tiles, ts, ctl,
                 c.has_init, init);
