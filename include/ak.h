@@ -121,12 +121,19 @@ typedef struct ak_opts {
     int32_t dims_shape;       /* ak_dims_shape */
     int32_t check;            /* 1: synchronize `stream` before returning and report
                                  device-side failures (AK_ERR_TIMEOUT) */
-    int32_t reserved0;
+    int32_t flags;            /* tuning switches, AK_FLAG_* (0 = none) */
     int64_t wait_limit_ns;    /* bound of each device-side wait of the scan; 0 = 1 s */
     int64_t debug_skip_publish_tile; /* fault injection for tests: the scan tile with this
                                  index never publishes its state, so its successors'
                                  bounded waits run out; -1 = off */
 } ak_opts;
+
+/* AK_FLAG_DIMS_CLUSTER: a strided dims reduction whose split fits 2..16
+ * blocks runs each output tile's blocks as one thread-block cluster and
+ * combines their partials in distributed shared memory (one kernel, no
+ * workspace partials) instead of a workspace and a second pass. Off by
+ * default: on GB300 the second pass measured faster at every tested shape. */
+#define AK_FLAG_DIMS_CLUSTER 1
 
 void ak_opts_default(ak_opts* opts);
 

@@ -60,7 +60,7 @@ def ak_kernel_launch_count() -> int:
 
 
 def make_opts(no_neutral=False, target_blocks=0, items_per_thread=0, dims_shape="auto", check=False,
-              wait_limit_ns=0, debug_skip_publish_tile=-1) -> _abi.ak_opts:
+              wait_limit_ns=0, debug_skip_publish_tile=-1, dims_cluster=False) -> _abi.ak_opts:
     o = _abi.ak_opts()
     lib().ak_opts_default(ctypes.byref(o))
     o.no_neutral = int(bool(no_neutral))
@@ -70,6 +70,7 @@ def make_opts(no_neutral=False, target_blocks=0, items_per_thread=0, dims_shape=
     o.check = int(bool(check))
     o.wait_limit_ns = int(wait_limit_ns)
     o.debug_skip_publish_tile = int(debug_skip_publish_tile)
+    o.flags = _abi.FLAG_DIMS_CLUSTER if dims_cluster else 0
     return o
 
 

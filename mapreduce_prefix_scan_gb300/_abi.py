@@ -19,6 +19,7 @@ MAPS = {"identity": 0, "abs": 1, "abs2": 2}
 OPS = {"add": 0, "mul": 1, "max": 2, "min": 3, "matmul": 4}
 STORES = {"overwrite": 0, "init": 1, "fold": 2}
 SHAPES = {"auto": 0, "thread": 1, "tiled": 2, "columns": 3}
+FLAG_DIMS_CLUSTER = 1
 
 # every symbol include/ak.h declares
 EXPORTS = ("ak_opts_default", "ak_status_string", "ak_dtype_size", "ak_last_cuda_error",
@@ -30,7 +31,7 @@ EXPORTS = ("ak_opts_default", "ak_status_string", "ak_dtype_size", "ak_last_cuda
 class ak_opts(ctypes.Structure):
     _fields_ = [("no_neutral", ctypes.c_int32), ("target_blocks", ctypes.c_int32),
                 ("items_per_thread", ctypes.c_int32), ("dims_shape", ctypes.c_int32),
-                ("check", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("check", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("wait_limit_ns", ctypes.c_int64), ("debug_skip_publish_tile", ctypes.c_int64)]
 
 

@@ -170,6 +170,7 @@ struct DimsCall {
     void* ws;
     size_t ws_bytes;
     int forced_shape;
+    bool allow_cluster;
     cudaStream_t stream;
     // general fallback (any dims mask): full shape and mask
     int ndim;

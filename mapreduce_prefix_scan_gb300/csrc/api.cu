@@ -405,6 +405,7 @@ ak_status setup_dims(const void* src, int ndim, const int64_t* shape, uint32_t m
     d->c.acc = acc;
     d->c.no_neutral = o.no_neutral != 0;
     d->c.forced_shape = o.dims_shape;
+    d->c.allow_cluster = (o.flags & AK_FLAG_DIMS_CLUSTER) != 0;
     d->c.ndim = ndim;
     d->c.mask = mask;
     for (int i = 0; i < ndim; ++i) d->c.shape[i] = shape[i];

@@ -110,14 +110,15 @@ def test_accumulate_validates_and_plans_on_host(L):
 
 def test_dims_selector(L):
     import mapreduce_prefix_scan_gb300 as ak
-    # 3072 x 2048 bf16, dims=2: 16-byte vectors of 8; the reduction is split
-    # over a cluster of at most 16 blocks and the device gets >= 1 block per SM
+    # 3072 x 2048 bf16, dims=2: 16-byte vectors of 8, a warp across a
+    # 256-output row segment, 8 row groups, the reduction split so that the
+    # device gets >= 1 block per SM
     shape, tile, groups, split = ak.ak_dims_select(3072, 2048, 1, 2, 8, 152)
-    assert shape == "columns" and tile % 8 == 0 and groups == 256 // (tile // 8) and 1 < split <= 16
+    assert shape == "columns" and tile == 256 and groups == 8 and split > 1
     assert -(-3072 // tile) * split >= 152
-    # middle dim of 64 x 4096 x 32 f32: tiles within the 64 outputs of a run
+    # middle dim of 64 x 4096 x 32 f32: 16 threads cover the 64 outputs of a run
     shape, tile, groups, split = ak.ak_dims_select(64, 4096, 32, 4, 4, 152)
-    assert shape == "columns" and 64 % tile == 0 and split <= 16
+    assert shape == "columns" and tile == 64 and groups == 16 and split > 1
     # short reductions take one thread per output vector
     assert ak.ak_dims_select(100_000, 16, 1, 4, 4, 152)[0] == "thread"
     # forced shapes are honoured

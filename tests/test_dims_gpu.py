@@ -45,10 +45,11 @@ def _check_float(x, kind, shape, dims, out, f="identity", init=None):
 # the strided workloads at full size
 # --------------------------------------------------------------------------
 
-def test_3072x2048_bf16_dims2():
+@pytest.mark.parametrize("cluster", [False, True])
+def test_3072x2048_bf16_dims2(cluster):
     shape = (3072, 2048)
     x = synth.normal_bf16_bits(3072 * 2048, seed=0, stream=40)
-    out = _run(x, "bf16", shape, [1])
+    out = _run(x, "bf16", shape, [1], opts=ak.make_opts(dims_cluster=cluster))
     assert out.dtype == torch.bfloat16 and out.shape == (1, 3072)
     _check_float(x, "bf16", shape, [1], out)
 
@@ -83,10 +84,10 @@ SHAPES3 = [(1000, 37, 3), (17, 3000, 2), (130, 129, 5), (4100, 65, 1), (5, 70_00
 
 
 @pytest.mark.parametrize("shape", SHAPES3)
-@pytest.mark.parametrize("forced", ["auto", "thread", "tiled", "columns"])
+@pytest.mark.parametrize("forced", ["auto", "thread", "tiled", "columns", "cluster"])
 def test_forced_shapes_f32_and_i64(shape, forced):
     n = int(np.prod(shape))
-    opts = ak.make_opts(dims_shape=forced)
+    opts = ak.make_opts(dims_cluster=True) if forced == "cluster" else ak.make_opts(dims_shape=forced)
     x = gen("f32", n, stream=44, dist="normal")
     _check_float(x, "f32", shape, [1], _run(x, "f32", shape, [1], opts=opts))
     xi = gen("i64", n, stream=45)
@@ -100,8 +101,9 @@ def test_forced_shapes_f32_and_i64(shape, forced):
 def test_bf16_outputs_ragged(shape):
     n = int(np.prod(shape))
     x = gen("bf16", n, stream=46)
-    for forced in ("auto", "thread", "columns"):
-        _check_float(x, "bf16", shape, [1], _run(x, "bf16", shape, [1], opts=ak.make_opts(dims_shape=forced)))
+    for forced in ("auto", "thread", "columns", "cluster"):
+        opts = ak.make_opts(dims_cluster=True) if forced == "cluster" else ak.make_opts(dims_shape=forced)
+        _check_float(x, "bf16", shape, [1], _run(x, "bf16", shape, [1], opts=opts))
 
 
 def test_misaligned_source_falls_back_to_scalar_rows():
@@ -118,8 +120,9 @@ def test_misaligned_source_falls_back_to_scalar_rows():
 def test_mat2_dims_in_order(shape):
     n = int(np.prod(shape))
     x = synth.mat2_modp(n, stream=48)
-    for forced in ("auto", "thread", "columns"):
-        got = _run(x, "mat2", shape, [1], op="matmul", opts=ak.make_opts(dims_shape=forced))
+    for forced in ("auto", "thread", "columns", "cluster"):
+        opts = ak.make_opts(dims_cluster=True) if forced == "cluster" else ak.make_opts(dims_shape=forced)
+        got = _run(x, "mat2", shape, [1], op="matmul", opts=opts)
         assert_exact(got.cpu().numpy().view(np.uint32).reshape(-1, 4),
                      oracle.reduce_dims(x, "mat2", shape, [1]))
 
