@@ -273,6 +273,7 @@ def _configs(ak, torch, dev, peak, flush_buf, reps):
         rec(name, lambda t: (lambda: ak.ak_accumulate(t, dst=y, workspace=w, **kw)), a, nbytes)
 
     scan_rec("cumsum_f64_1e8", synth.uniform_f64_01(N_BIG, 0, 60), (N_BIG,), 16 * N_BIG)
+    scan_rec("cumsum_f32_1e8", synth.normal_f32(N_BIG, 0, 65), (N_BIG,), 8 * N_BIG)
     scan_rec("accumulate_max_optional_f32_1e7", synth.normal_f32(10**7, 0, 61), (10**7,), 8 * 10**7, op="max",
              opts=ak.make_opts(no_neutral=True))
     scan_rec("cumsum_dims1_4096x4096_f32", synth.normal_f32(4096 * 4096, 0, 62), (4096, 4096), 8 * 4096 * 4096,
@@ -537,6 +538,10 @@ def run_profile(case: str):
         x = torch.from_numpy(synth.uniform_f64_01(2 * 10**7, 0, 60)).to(dev)
         y = torch.empty_like(x)
         fn = lambda: ak.ak_accumulate(x, dst=y)
+    elif case == "scan_f32":  # 1e8 f32 cumsum: 400 MB in, 400 MB out
+        x = torch.from_numpy(synth.normal_f32(10**8, 0, 65)).to(dev)
+        y = torch.empty_like(x)
+        fn = lambda: ak.ak_accumulate(x, dst=y)
     elif case == "scan_max":  # 1e7 f32 max, Optional partials
         x = torch.from_numpy(synth.normal_f32(10**7, 0, 61)).to(dev)
         y = torch.empty_like(x)
@@ -571,7 +576,7 @@ def main():
     ap.add_argument("--config-reps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--small", action="store_true", help="n = 1e6 (quick runs)")
-    ap.add_argument("--profile", default=None, help="run a small ncu case: reduce|scan|scan_max|scan_mat2|dims|dims_big")
+    ap.add_argument("--profile", default=None, help="run a small ncu case: reduce|scan|scan_f32|scan_max|scan_mat2|dims|dims_big")
     args = ap.parse_args()
     if args.profile:
         run_profile(args.profile)

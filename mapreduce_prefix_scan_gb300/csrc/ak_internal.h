@@ -218,8 +218,14 @@ struct ScanPlan {
     int grid;
     int64_t tiles_per_line, tiles;
     size_t state_off, ws_bytes;
+    // kind 0 only: the TMA tile scan applies (one element type throughout,
+    // 128-byte rows); it is tried first and the super-tile scan is the
+    // fallback (unaligned pointers), so ws_bytes covers both
+    bool tma;
+    int64_t tma_tiles_per_line, tma_tiles;
+    size_t tma_ws_bytes;
 };
-ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_dtype acc,
+ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_dtype acc, ak_dtype out,
                     ak_op op, bool no_neutral, int target_blocks, int items,
                     const DeviceInfo& dev, ScanPlan* plan);
 ak_status run_scan(const ScanCall& c, const ScanPlan& plan);

@@ -546,7 +546,9 @@ extern "C" ak_status ak_accumulate_workspace_size(int ndim, const int64_t* shape
     const ak_opts o = resolve_opts(opts);
     DeviceInfo dev = {};
     ScanPlan p;
-    s = plan_scan(inner, len, outer, in, acc, op, o.no_neutral != 0, o.target_blocks, o.items_per_thread, dev, &p);
+    // the output type is not part of this query: planning with out = acc
+    // covers the largest workspace any output type can need
+    s = plan_scan(inner, len, outer, in, acc, acc, op, o.no_neutral != 0, o.target_blocks, o.items_per_thread, dev, &p);
     if (s != AK_OK) return s;
     *bytes = p.ws_bytes;
     return AK_OK;
@@ -573,7 +575,7 @@ extern "C" ak_status ak_accumulate(const void* src, void* dst, int ndim, const i
     DeviceInfo dev;
     if (!current_device(&dev)) return AK_ERR_CUDA;
     ScanPlan p;
-    s = plan_scan(inner, len, outer, in, acc, op, o.no_neutral != 0, o.target_blocks, o.items_per_thread, dev, &p);
+    s = plan_scan(inner, len, outer, in, acc, out, op, o.no_neutral != 0, o.target_blocks, o.items_per_thread, dev, &p);
     if (s != AK_OK) return s;
     if (!ws || ws_bytes < p.ws_bytes || !aligned(ws, 16)) return AK_ERR_WORKSPACE;
     ScanCall c;

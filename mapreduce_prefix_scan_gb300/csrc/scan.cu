@@ -31,9 +31,14 @@
 // the epoch in the workspace's error word, which every other waiter also
 // watches, and all blocks leave early.
 #include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "ak_common.cuh"
 #include "ak_internal.h"
+#include "ak_tma.cuh"
 
 namespace ak {
 
@@ -52,14 +57,21 @@ template <class Acc>
 constexpr int default_block() {
     return sizeof(Acc) >= 16 ? 128 : 256;
 }
-// Elements of one thread's segment in the long-line scan: 512 bytes of
-// 4- and 8-byte elements, 1 KB of 16-byte ones (128 KB super-tiles).
+// Elements of one thread's segment in the long-line scan: 256 bytes of
+// 4-byte elements (64 KB super-tiles), 512 bytes of 8-byte ones and 1 KB of
+// 16-byte ones (128 KB super-tiles: more operator work per byte, so more
+// bytes per look-back).
 template <class Acc>
 constexpr int default_seg() {
-    return sizeof(Acc) >= 16 ? 64 : (sizeof(Acc) == 8 ? 64 : 128);
+    return sizeof(Acc) >= 16 ? 64 : (sizeof(Acc) == 8 ? 64 : 64);
 }
 // Predecessor super-tiles one look-back round inspects, per thread.
 constexpr int kLookSlots = 2;
+// TMA tile scan: threads per block (one 128-byte row each, so a tile is
+// kTmaBlock * 128 bytes) and tiles staged per block (the one being scanned,
+// the one folded ahead of it, and the copies in flight).
+constexpr int kTmaBlock = 256;
+constexpr int kTmaStages = 3;
 // Resident blocks per SM the register budget is sized for: 3 blocks of 256
 // threads (<= 80 registers a thread), a quarter of the thread slots for
 // 16-byte elements.
@@ -149,31 +161,79 @@ __device__ __forceinline__ uint64_t rec_check(uint64_t tag, const P& v) {
     return h ^ (h >> 29);
 }
 
-// Relaxed, L2-coherent word access of the records (never cached in L1, never
-// hoisted out of a polling loop).
-__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+
+// A whole record as 64-bit words, moved with vector accesses: one 32-byte
+// access for the 32-byte records (partials of up to 16 bytes), 16-byte
+// accesses otherwise. One request per record instead of one per word; a
+// read that races a rewrite may still mix old and new words, which the
+// check word rejects.
+template <class P>
+constexpr int rec_words() {
+    return (int)(sizeof(TileRec<P>) / 8);
 }
-__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+template <class P>
+__device__ __forceinline__ void rec_load(const TileRec<P>* r, uint64_t (&w)[rec_words<P>()]) {
+    constexpr int NW = rec_words<P>();
+    const uint64_t* p = reinterpret_cast<const uint64_t*>(r);
+    if constexpr (NW == 4) {
+        asm volatile("ld.relaxed.gpu.global.v4.u64 {%0,%1,%2,%3}, [%4];"
+                     : "=l"(w[0]), "=l"(w[1]), "=l"(w[2]), "=l"(w[3])
+                     : "l"(p)
+                     : "memory");
+    } else {
+        static_assert(NW % 2 == 0, "records are whole 16-byte units");
+#pragma unroll
+        for (int i = 0; i < NW; i += 2)
+            asm volatile("ld.relaxed.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(w[i]), "=l"(w[i + 1]) : "l"(p + i) : "memory");
+    }
 }
-__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
-    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+template <class P>
+__device__ __forceinline__ void rec_store(TileRec<P>* r, const uint64_t (&w)[rec_words<P>()]) {
+    constexpr int NW = rec_words<P>();
+    uint64_t* p = reinterpret_cast<uint64_t*>(r);
+    if constexpr (NW == 4) {
+        asm volatile("st.relaxed.gpu.global.v4.u64 [%0], {%1,%2,%3,%4};" ::"l"(p), "l"(w[0]), "l"(w[1]), "l"(w[2]),
+                     "l"(w[3])
+                     : "memory");
+    } else {
+#pragma unroll
+        for (int i = 0; i < NW; i += 2)
+            asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1,%2};" ::"l"(p + i), "l"(w[i]), "l"(w[i + 1]) : "memory");
+    }
+}
+// Status for this call (0 when not valid) and value of a record's words.
+template <class P>
+__device__ __forceinline__ uint64_t rec_decode(const uint64_t (&w)[rec_words<P>()], uint64_t epoch, P* v) {
+    memcpy(v, &w[2], sizeof(P));
+    const uint64_t tag = w[0];
+    if ((tag >> 2) != epoch || w[1] != rec_check(tag, *v)) return 0;
+    return tag & 3u;
 }
 
 // Reads a record: its status for this call (0 when not valid) and value.
 template <class P>
 __device__ __forceinline__ uint64_t read_rec(const TileRec<P>* r, uint64_t epoch, P* v) {
-    const uint64_t tag = ld_relaxed_u64(&r->tag);
-    const uint64_t chk = ld_relaxed_u64(&r->chk);
-    uint32_t* w = reinterpret_cast<uint32_t*>(v);
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(&r->v);
+    uint64_t w[rec_words<P>()];
+    rec_load(r, w);
+    return rec_decode<P>(w, epoch, v);
+}
+
+// The records of one look-back window as raw words, read ahead of their
+// use (the loads are in flight while the block does other work) and
+// validated when they are consumed.
+template <class P, int S>
+struct LookWin {
+    uint64_t w[S][rec_words<P>()];
+};
+
+template <class P, int S>
+__device__ __forceinline__ void look_issue(LookWin<P, S>& w, const TileRec<P>* recs, int64_t base, int64_t g_first) {
 #pragma unroll
-    for (int i = 0; i < (int)(sizeof(P) / 4); ++i) w[i] = ld_relaxed_u32(src + i);
-    if ((tag >> 2) != epoch || chk != rec_check(tag, *v)) return 0;
-    return tag & 3u;
+    for (int k = 0; k < S; ++k) {
+#pragma unroll
+        for (int i = 0; i < rec_words<P>(); ++i) w.w[k][i] = 0;
+        if (base + k >= g_first) rec_load(recs + base + k, w.w[k]);
+    }
 }
 
 struct ScanCtl {
@@ -223,15 +283,17 @@ __device__ __forceinline__ typename M::P block_reduce_ordered(typename M::P v, t
 // back. The window is wide enough that the published-prefix frontier keeps
 // up with the rate at which tiles start. Returns false (in every thread)
 // when a wait ran out or another block gave up.
-template <class M, int BLOCK>
+template <class M, int BLOCK, int SLOTS = kLookSlots, bool FAST = true>
 __device__ __forceinline__ bool look_back(int64_t g, int64_t g_first, const TileState<typename M::P>& ts,
                                           const ScanCtl& ctl, typename M::P* red, int* ints,
-                                          typename M::P* excl0) {
+                                          typename M::P* excl0,
+                                          const LookWin<typename M::P, SLOTS>* pre = nullptr) {
     using P = typename M::P;
-    constexpr int W = BLOCK / kWarp, S = kLookSlots, WIN = S * BLOCK;
+    constexpr int W = BLOCK / kWarp, S = SLOTS, WIN = S * BLOCK;
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
     // Fast path: warp 0 reads the 32 nearest records once; when an inclusive
     // prefix is among them and every newer one has published, that decides.
+    if constexpr (FAST) {
     if (warp == 0) {
         const int64_t idx = g - kWarp + lane;
         const bool valid = idx >= g_first;
@@ -249,6 +311,7 @@ __device__ __forceinline__ bool look_back(int64_t g, int64_t g_first, const Tile
     }
     __syncthreads();
     if (ints[2 * kWarp]) return true;
+    }
 
     P excl = M::empty();
     int64_t hi = g - 1;
@@ -257,11 +320,25 @@ __device__ __forceinline__ bool look_back(int64_t g, int64_t g_first, const Tile
         const int64_t base = hi - (WIN - 1) + (int64_t)S * tid;  // this thread's first slot
         uint64_t st[S];
         P val[S];
+        if (pre != nullptr && hi == g - 1) {
+            // the first window was read ahead: validate those words now
 #pragma unroll
-        for (int k = 0; k < S; ++k) {
-            st[k] = 0;
-            val[k] = M::empty();
-            if (base + k >= g_first) st[k] = read_rec(ts.recs + base + k, ctl.epoch, &val[k]);
+            for (int k = 0; k < S; ++k) {
+                st[k] = 0;
+                val[k] = M::empty();
+                if (base + k >= g_first) {
+                    P v;
+                    st[k] = rec_decode<P>(pre->w[k], ctl.epoch, &v);
+                    if (st[k] != 0) val[k] = v;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < S; ++k) {
+                st[k] = 0;
+                val[k] = M::empty();
+                if (base + k >= g_first) st[k] = read_rec(ts.recs + base + k, ctl.epoch, &val[k]);
+            }
         }
         // nearest inclusive prefix seen so far: the highest window position
         int mine = -1;
@@ -323,14 +400,14 @@ __device__ __forceinline__ bool look_back(int64_t g, int64_t g_first, const Tile
 template <class P>
 __device__ __forceinline__ void publish(const TileState<P>& ts, int64_t g, uint64_t status, const P& v,
                                         uint64_t epoch) {
-    TileRec<P>* r = ts.recs + g;
     const uint64_t tag = (epoch << 2) | status;
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(&r->v);
+    uint64_t w[rec_words<P>()];
 #pragma unroll
-    for (int i = 0; i < (int)(sizeof(P) / 4); ++i) st_relaxed_u32(dst + i, w[i]);
-    st_relaxed_u64(&r->chk, rec_check(tag, v));
-    st_relaxed_u64(&r->tag, tag);
+    for (int i = 0; i < rec_words<P>(); ++i) w[i] = 0;
+    w[0] = tag;
+    w[1] = rec_check(tag, v);
+    memcpy(&w[2], &v, sizeof(P));
+    rec_store(ts.recs + g, w);
 }
 
 // ---------------------------------------------------------------------------
@@ -669,6 +746,346 @@ __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Ac
     }
 }
 
+// ---------------------------------------------------------------------------
+// TMA tile scan: one read and one write of every element
+// ---------------------------------------------------------------------------
+
+// Shared memory of one block: the staged tiles, plus slack to align them to
+// the 1024 bytes that the 128-byte swizzle pattern repeats over.
+template <int BLOCK, int STAGES>
+constexpr int tma_smem_bytes() {
+    return STAGES * BLOCK * 128 + 1024;
+}
+// Resident blocks per SM the register budget is sized for (as many as the
+// staged tiles leave room for in the SM's 228 KB of shared memory).
+template <int BLOCK, int STAGES>
+constexpr int tma_min_blocks() {
+    return (228 * 1024) / (tma_smem_bytes<BLOCK, STAGES>() + 2048) < 1
+               ? 1
+               : (228 * 1024) / (tma_smem_bytes<BLOCK, STAGES>() + 2048);
+}
+
+// Row r of a swizzled tile <-> the R elements of a thread, 16 bytes at a time.
+template <class T, int R>
+__device__ __forceinline__ void row_load(T (&run)[R], const unsigned char* buf, int r) {
+    static_assert(R * sizeof(T) == 128 && sizeof(T) % 4 == 0 && sizeof(T) <= 16, "128-byte rows of word-sized elements");
+    constexpr int WPE = sizeof(T) / 4, E = 16 / sizeof(T);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint4 v = *reinterpret_cast<const uint4*>(buf + swz128(r, j));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < E; ++k) {
+            uint32_t e[WPE];
+#pragma unroll
+            for (int q = 0; q < WPE; ++q) e[q] = w[k * WPE + q];
+            memcpy(&run[j * E + k], e, sizeof(T));
+        }
+    }
+}
+template <class T, int R>
+__device__ __forceinline__ void row_store(unsigned char* buf, int r, const T (&run)[R]) {
+    constexpr int WPE = sizeof(T) / 4, E = 16 / sizeof(T);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < E; ++k) {
+            uint32_t e[WPE];
+            memcpy(e, &run[j * E + k], sizeof(T));
+#pragma unroll
+            for (int q = 0; q < WPE; ++q) w[k * WPE + q] = e[q];
+        }
+        *reinterpret_cast<uint4*>(buf + swz128(r, j)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// A thread's row straight to global memory: 32-byte stores when the row is
+// 32-byte aligned, else 16-byte ones; the L2 is told this is a last use.
+template <class T, int R>
+__device__ __forceinline__ void row_store_global(T* dst, const T (&run)[R], uint64_t policy) {
+    static_assert(R * sizeof(T) == 128, "128-byte rows");
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(run);
+    if (reinterpret_cast<uintptr_t>(dst) % 32 == 0) {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            Raw<32> r;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) r.w[q] = w[8 * h + q];
+            st_hint32(reinterpret_cast<char*>(dst) + 32 * h, r, policy);
+        }
+    } else {
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+            Raw<16> r;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) r.w[q] = w[4 * h + q];
+            st_hint16(reinterpret_cast<char*>(dst) + 16 * h, r, policy);
+        }
+    }
+}
+
+// Fold of a whole row: in element order, or for a commutative operator as
+// four interleaved chains combined at the end (independent operations in
+// flight; a reordering that only rounding can tell apart).
+template <class M, class T, int R>
+__device__ __forceinline__ T row_fold(const T (&run)[R]) {
+    if constexpr (M::commutative && R % 4 == 0) {
+        T c[4] = {run[0], run[1], run[2], run[3]};
+#pragma unroll
+        for (int i = 4; i < R; i += 4) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) c[q] = M::op::apply(c[q], run[i + q]);
+        }
+        return M::op::apply(M::op::apply(c[0], c[1]), M::op::apply(c[2], c[3]));
+    } else {
+        T a = run[0];
+#pragma unroll
+        for (int i = 1; i < R; ++i) a = M::op::apply(a, run[i]);
+        return a;
+    }
+}
+
+// Inclusive scan of a row in place, starting from the exclusive prefix
+// `mine` (absent only for the very first row of a line without init).
+template <class M, class T, int R>
+__device__ __forceinline__ void row_scan_from(T (&run)[R], const typename M::P& mine) {
+    T a = M::present(mine) ? M::op::apply(M::value(mine), run[0]) : run[0];
+    run[0] = a;
+#pragma unroll
+    for (int i = 1; i < R; ++i) {
+        a = M::op::apply(a, run[i]);
+        run[i] = a;
+    }
+}
+
+// Long contiguous lines, element type = accumulator type = output type,
+// viewed as rows of 128 bytes (R elements): a tile is BLOCK rows and thread
+// t owns row t. A persistent block works through the tiles it claims (in
+// claim order) with a ring of STAGES shared-memory stages: in round n it
+// scans tile n, holds tile n+1 (already folded, its aggregate published)
+// and has the copies of tiles n+2 .. n+STAGES-1 in flight. Thread 0 claims
+// tile indices from the call's counter (one claim in flight ahead of its
+// use) and has each tile copied by one bulk tensor load, swizzled so that
+// every thread reads its own row without bank conflicts.
+//
+// Round n: refill the stage freed by round n-1 with the next claimed tile;
+// fold tile n+1 -- every thread folds its row, the row totals are scanned
+// across the block, the tile's aggregate is published (a line's first tile:
+// its inclusive prefix) and each thread keeps its exclusive in-tile prefix;
+// look back to tile n's exclusive prefix (decoupled look-back over the
+// fence-free tile records) and publish its inclusive prefix; every thread
+// reads its row of tile n again, scans it from its exclusive prefix and
+// writes it back in place; one bulk tensor store writes the tile out.
+// Because a tile's aggregate is published one round before its own look-
+// back, look-backs find their predecessors published instead of waiting on
+// them (the same deferral as the super-tile scan, with the tile held in
+// shared memory rather than in L2). HBM traffic is one read and one write of
+// every element; the operator is applied twice per element, as in any
+// single-pass scan whose tiles cannot wait for their prefix before
+// starting. Rows past a line's end are zero-filled by the copy and ignored;
+// the partial row of a single ragged line is read and written directly by
+// its thread.
+template <class T, class M, int BLOCK, int STAGES>
+__global__ void __launch_bounds__(BLOCK, (tma_min_blocks<BLOCK, STAGES>()))
+    k_scan_tma(const __grid_constant__ CUtensorMap tin, const T* __restrict__ x, T* __restrict__ y, int64_t len,
+               int64_t rows_full, int64_t tiles_per_line, int64_t ntiles, TileState<typename M::P> ts, ScanCtl ctl,
+               bool has_init, T init) {
+    static_assert(STAGES >= 3, "a stage scanned, a stage folded, at least one copy in flight");
+    constexpr int LS = 512 / BLOCK > kLookSlots ? 512 / BLOCK : kLookSlots;  // look-back window: LS * BLOCK tiles
+    using P = typename M::P;
+    constexpr int R = 128 / (int)sizeof(T);
+    constexpr int W = BLOCK / kWarp;
+    constexpr uint32_t TILE_BYTES = BLOCK * 128;
+    extern __shared__ unsigned char dyn_smem[];
+    unsigned char* const bufs =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t full[STAGES];
+    __shared__ int64_t s_k[STAGES];
+    __shared__ P warp_tot[W];
+    __shared__ P red[W];
+    __shared__ int ints[2 * kWarp + 1];
+    __shared__ P s_bc;
+    const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    const int64_t rem = len - rows_full * R;  // elements of the partial last row (a single line only)
+
+    // valid elements of this thread's row of tile k
+    auto row_count = [&](int64_t k) -> int {
+        const int64_t row = (k % tiles_per_line) * BLOCK + tid;
+        return row < rows_full ? R : (row == rows_full ? (int)rem : 0);
+    };
+    auto row_src = [&](int64_t k) -> int64_t {
+        return (k / tiles_per_line) * len + ((k % tiles_per_line) * BLOCK + tid) * R;
+    };
+    // thread 0: start the copy of tile k into stage s; a tile holding only
+    // the partial row needs no copy, and a plain arrival completes the stage
+    auto issue = [&](int64_t k, int s) {
+        const int64_t row0 = (k % tiles_per_line) * BLOCK;
+        if (row0 < rows_full) {
+            mbar_arrive_expect_tx(&full[s], TILE_BYTES);
+            tma_load_3d(bufs + (size_t)s * TILE_BYTES, &tin, 0, (int)row0, (int)(k / tiles_per_line), &full[s]);
+        } else {
+            mbar_arrive(&full[s]);
+        }
+    };
+    // thread 0, after a failure: let the copies of ring slots first..last
+    // that were started land before the block leaves (each wait bounded)
+    auto drain = [&](int first, int last) {
+        const uint64_t until = globaltimer_ns() + (uint64_t)ctl.wait_limit_ns;
+        for (int j = first; j <= last; ++j) {
+            const int s = j % STAGES;
+            if (s_k[s] < ntiles) mbar_wait(&full[s], (uint32_t)(j / STAGES) & 1u, until);
+        }
+    };
+    auto give_up = [&](int first, int last) {
+        if (tid == 0) {
+            atomicExch(reinterpret_cast<unsigned long long*>(ctl.error_word), (unsigned long long)ctl.epoch);
+            drain(first, last);
+        }
+    };
+    // every thread: wait for ring slot j's copy (bounded); false in all
+    // threads when any thread's wait ran out
+    auto landed = [&](int j) -> bool {
+        const bool ok = mbar_wait(&full[j % STAGES], (uint32_t)(j / STAGES) & 1u,
+                                  globaltimer_ns() + (uint64_t)ctl.wait_limit_ns);
+        return !__syncthreads_or(!ok);
+    };
+    // every thread: fold its row of tile k (ring slot j) and scan the row
+    // totals across the block; returns the thread's exclusive prefix within
+    // the tile, and in thread 0 *agg = the tile's aggregate, which it
+    // publishes (the first tile of a line: as its inclusive prefix)
+    auto fold_tile = [&](int64_t k, int j, P* agg) -> P {
+        const int nt = row_count(k);
+        P tot = M::empty();
+        if (nt == R) {
+            T run[R];
+            row_load(run, bufs + (size_t)(j % STAGES) * TILE_BYTES, tid);
+            tot = M::lift(row_fold<M>(run));
+        } else if (nt > 0) {
+            const T* src = x + row_src(k);
+            for (int i = 0; i < nt; ++i) tot = M::combine(tot, M::lift(src[i]));
+        }
+        const P inc = warp_inclusive_scan<M>(tot, lane);
+        P lane_excl = shfl_up_any(inc, 1);
+        if (lane == 0) lane_excl = M::empty();
+        if (lane == kWarp - 1) warp_tot[warp] = inc;
+        __syncthreads();
+        if (warp == 0) {
+            const P w = lane < W ? warp_tot[lane] : M::empty();
+            const P wi = warp_inclusive_scan<M>(w, lane);
+            P we = shfl_up_any(wi, 1);
+            if (lane == 0) we = M::empty();
+            if (lane < W) warp_tot[lane] = we;
+            const P a = shfl_idx_any(wi, W - 1);
+            if (lane == 0) *agg = a;
+        }
+        __syncthreads();
+        const P mine = M::combine(warp_tot[warp], lane_excl);
+        if (tid == 0) {
+            const int64_t t = k % tiles_per_line;
+            if (tiles_per_line > 1 && t != tiles_per_line - 1 && k != ctl.skip_tile) {
+                if (t == 0) publish(ts, k, kStatusPrefix, M::combine(has_init ? M::lift(init) : M::empty(), *agg), ctl.epoch);
+                else publish(ts, k, kStatusAggregate, *agg, ctl.epoch);
+            }
+        }
+        __syncthreads();  // warp_tot is reused by the next fold
+        return mine;
+    };
+
+    unsigned long long next_claim = 0;
+    if (tid == 0) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+        tma_prefetch_map(&tin);
+        for (int s = 0; s < STAGES - 1; ++s) {
+            const int64_t k = claim_tile(ctl, ntiles);
+            s_k[s] = k;
+            if (k < ntiles) issue(k, s);
+        }
+        next_claim = atomicAdd(ctl.counter, 1ull);
+    }
+    __syncthreads();
+    if (s_k[0] >= ntiles) return;  // claims only grow: nothing was started
+    if (!landed(0)) {
+        give_up(0, STAGES - 2);
+        return;
+    }
+    P agg = M::empty();  // meaningful in thread 0
+    P mine = fold_tile(s_k[0], 0, &agg);
+    const uint64_t last_use = l2_policy_evict_first();
+
+    for (int n = 0;; ++n) {
+        const int b = n % STAGES;
+        const int64_t k = s_k[b];
+        if (tid == 0) {
+            // refill the stage freed by the previous round with the next claimed tile
+            const int bl = (n + STAGES - 1) % STAGES;
+            const int64_t kn = (int64_t)next_claim;
+            next_claim = atomicAdd(ctl.counter, 1ull);
+            s_k[bl] = kn;
+            if (kn < ntiles) issue(kn, bl);
+        }
+        // read tile k's look-back window now; the fold below hides the latency
+        const int64_t t = k % tiles_per_line;
+        LookWin<P, LS> win;
+        if (t != 0) look_issue(win, ts.recs, (k - 1) - (LS * BLOCK - 1) + (int64_t)LS * tid, k - t);
+
+        // fold the next tile: its aggregate goes out a round before its look-back
+        const int64_t k1 = s_k[(n + 1) % STAGES];
+        P agg1 = M::empty();
+        P mine1 = M::empty();
+        if (k1 < ntiles) {
+            if (!landed(n + 1)) {
+                give_up(n + 1, n + STAGES - 1);
+                return;
+            }
+            mine1 = fold_tile(k1, n + 1, &agg1);
+        }
+
+        // tile k's exclusive prefix
+        P prefix = has_init ? M::lift(init) : M::empty();
+        if (t != 0) {
+            if (!look_back<M, BLOCK, LS, false>(k, k - t, ts, ctl, red, ints, &prefix, &win)) {
+                give_up(n + 2, n + STAGES - 1);
+                return;  // uniform: every thread got the same answer
+            }
+            if (tid == 0) {
+                if (t != tiles_per_line - 1 && k != ctl.skip_tile)
+                    publish(ts, k, kStatusPrefix, M::combine(prefix, agg), ctl.epoch);
+                s_bc = prefix;
+            }
+            __syncthreads();
+            prefix = s_bc;
+        }
+
+        // scan the row from the thread's exclusive prefix and store it
+        unsigned char* const buf = bufs + (size_t)b * TILE_BYTES;
+        const int nt = row_count(k);
+        const P from = M::combine(prefix, mine);
+        if (nt == R) {
+            T run[R];
+            row_load(run, buf, tid);
+            row_scan_from<M>(run, from);
+            row_store_global(y + row_src(k), run, last_use);
+        } else if (nt > 0) {
+            const T* src = x + row_src(k);
+            T* dst = y + row_src(k);
+            P a = from;
+            for (int i = 0; i < nt; ++i) {
+                a = M::combine(a, M::lift(src[i]));
+                dst[i] = M::value(a);
+            }
+        }
+        // the stage is refilled next round: every thread is done reading it
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (k1 >= ntiles) break;  // claims only grow: nothing further was started
+        agg = agg1;
+        mine = mine1;
+    }
+}
+
 // Lines that fit one tile: block b scans line b with the init prefix; no
 // state is shared between blocks.
 template <class In, class Acc, class Out, class M, int ITEMS, int BLOCK>
@@ -719,6 +1136,100 @@ __global__ void __launch_bounds__(256) k_scan_strided(const In* __restrict__ x, 
     }
 }
 
+// cuTensorMapEncodeTiled from the driver the runtime is using (no link-time
+// dependency on libcuda); null when the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Lines of `rows` 128-byte rows (32 words), `lines` of them `line_bytes`
+// apart, copied in boxes of box_rows rows with the 128-byte swizzle.
+bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const void* base, int64_t rows,
+                 int64_t lines, uint64_t line_bytes, int box_rows) {
+    const cuuint64_t dims[3] = {32, (cuuint64_t)rows, (cuuint64_t)lines};
+    const cuuint64_t strides[2] = {128, (cuuint64_t)line_bytes};
+    const cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Per device: the kernel's shared-memory opt-in done and its resident
+// blocks per SM (0 = not yet known).
+template <class T, class M>
+int tma_blocks_per_sm(int device) {
+    static std::atomic<int> cache[64];
+    auto kernel = k_scan_tma<T, M, kTmaBlock, kTmaStages>;
+    constexpr int smem = tma_smem_bytes<kTmaBlock, kTmaStages>();
+    if (device >= 0 && device < 64) {
+        const int v = cache[device].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kTmaBlock, smem) != cudaSuccess) return -1;
+    if (occ < 1) return 0;
+    if (device >= 0 && device < 64) cache[device].store(occ, std::memory_order_relaxed);
+    return occ;
+}
+
+// The TMA tile scan; AK_ERR_UNSUPPORTED (nothing launched) when the
+// pointers are not 16-byte aligned or the driver has no tensor-map encoder.
+template <class T, class M>
+ak_status launch_tma(const ScanCall& c, const ScanPlan& p) {
+    constexpr int64_t R = 128 / (int64_t)sizeof(T);
+    if (reinterpret_cast<uintptr_t>(c.src) % 16 != 0 || reinterpret_cast<uintptr_t>(c.dst) % 16 != 0)
+        return AK_ERR_UNSUPPORTED;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return AK_ERR_UNSUPPORTED;
+    const int64_t rows_full = c.len / R;
+    const uint64_t line_bytes = c.outer > 1 ? (uint64_t)c.len * sizeof(T) : (uint64_t)rows_full * 128;
+    alignas(64) CUtensorMap tin;
+    if (!encode_rows(enc, &tin, c.src, rows_full, c.outer, line_bytes, kTmaBlock)) return AK_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    if (!current_device(&dev)) return AK_ERR_CUDA;
+    const int occ = tma_blocks_per_sm<T, M>(dev.device);
+    if (occ < 0) return cuda_fail(cudaGetLastError());
+    if (occ == 0) return AK_ERR_UNSUPPORTED;
+    int64_t grid = std::min<int64_t>(p.tma_tiles, (int64_t)occ * dev.sm_count);
+    if (c.target_blocks > 0) grid = std::min<int64_t>(grid, c.target_blocks);
+    char* ws = static_cast<char*>(c.ws);
+    TileState<typename M::P> ts;
+    ts.recs = reinterpret_cast<TileRec<typename M::P>*>(ws + p.state_off);
+    ScanCtl ctl;
+    ctl.epoch = c.epoch;
+    ctl.error_word = reinterpret_cast<uint64_t*>(ws);  // WsHeader::error_word
+    ctl.counter = reinterpret_cast<unsigned long long*>(ws + 64);
+    ctl.wait_limit_ns = c.wait_limit_ns;
+    ctl.skip_tile = c.skip_tile;
+    T init;
+    memcpy(&init, c.init.b, sizeof(T));
+    // fresh counter, error word and records (correct under CUDA graph replay)
+    cudaError_t e = cudaMemsetAsync(ws, 0, p.tma_ws_bytes, c.stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    k_scan_tma<T, M, kTmaBlock, kTmaStages><<<(unsigned)grid, kTmaBlock, tma_smem_bytes<kTmaBlock, kTmaStages>(),
+                                               c.stream>>>(tin, static_cast<const T*>(c.src),
+                                                           static_cast<T*>(c.dst), c.len, rows_full,
+                                                           p.tma_tiles_per_line, p.tma_tiles, ts, ctl, c.has_init,
+                                                           init);
+    ak_status s = check_launch();
+    if (s == AK_OK) count_launches(1);
+    return s;
+}
+
 template <class In, class Acc, class Out, class M>
 ak_status launch(const ScanCall& c, const ScanPlan& p) {
     using P = typename M::P;
@@ -741,6 +1252,13 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
         return AK_ERR_UNSUPPORTED;
     } else {
         if (p.block != BLOCK || p.items != ITEMS) return AK_ERR_UNSUPPORTED;
+        if constexpr (std::is_same_v<In, Acc> && std::is_same_v<Acc, Out> &&
+                      (sizeof(Acc) == 4 || sizeof(Acc) == 8 || sizeof(Acc) == 16)) {
+            if (p.kind == 0 && p.tma) {
+                const ak_status st = launch_tma<Acc, M>(c, p);
+                if (st != AK_ERR_UNSUPPORTED) return st;
+            }
+        }
         char* ws = static_cast<char*>(c.ws);
         TileState<P> ts;
         ts.recs = reinterpret_cast<TileRec<P>*>(ws + p.state_off);
@@ -787,7 +1305,7 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
 
 }  // namespace
 
-ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_dtype acc, ak_op op,
+ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_dtype acc, ak_dtype out, ak_op op,
                     bool no_neutral, int target_blocks, int items, const DeviceInfo& dev, ScanPlan* p) {
     (void)op;
     (void)target_blocks;
@@ -800,6 +1318,10 @@ ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_d
     p->tiles = 0;
     p->tiles_per_line = 0;
     p->grid = 0;
+    p->tma = false;
+    p->tma_tiles_per_line = 0;
+    p->tma_tiles = 0;
+    p->tma_ws_bytes = 0;
     if (inner > 1) {
         p->kind = 1;
         p->block = 256;
@@ -811,7 +1333,7 @@ ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_d
     if (items != 0 && items != it) return AK_ERR_UNSUPPORTED;
     p->items = it;
     const int block = asz >= 16 ? 128 : 256;
-    const int seg = asz >= 16 ? 64 : (asz == 8 ? 64 : 128);
+    const int seg = asz >= 16 ? 64 : (asz == 8 ? 64 : 64);
     p->block = block;
     const int64_t tile = (int64_t)block * it;
     if (len <= tile) {
@@ -824,6 +1346,20 @@ ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_d
     p->tiles_per_line = (len + super - 1) / super;
     p->tiles = p->tiles_per_line * outer;
     p->ws_bytes = align_up(kWsHeader + (size_t)p->tiles * (16 + align_up(psz, 16)), 256);  // TileRec per super-tile
+    // TMA tile scan: one integer element type (the floating-point and matrix
+    // scans do more operator work per byte and run faster as super-tiles),
+    // rows of 128 bytes, several tiles per line, and lines that start on a
+    // row boundary unless there is only one
+    const int64_t rl = 128 / (int64_t)asz;
+    if (items == 0 && in == acc && out == acc && (acc == AK_I32 || acc == AK_I64) && len > kTmaBlock * rl &&
+        (outer == 1 || len % rl == 0) && len / rl < ((int64_t)1 << 31) && outer < ((int64_t)1 << 31)) {
+        const int64_t rows = (len + rl - 1) / rl;
+        p->tma = true;
+        p->tma_tiles_per_line = (rows + kTmaBlock - 1) / kTmaBlock;
+        p->tma_tiles = p->tma_tiles_per_line * outer;
+        p->tma_ws_bytes = align_up(kWsHeader + (size_t)p->tma_tiles * (16 + align_up(psz, 16)), 256);
+        p->ws_bytes = std::max(p->ws_bytes, p->tma_ws_bytes);
+    }
     return AK_OK;
 }
 

@@ -17,7 +17,7 @@ import torch
 import mapreduce_prefix_scan_gb300 as ak
 import oracle
 import synth
-from helpers import F64_REL, assert_close_f32, assert_exact, dev_of, gen
+from helpers import F32_REL, F64_REL, assert_close_f32, assert_exact, dev_of, gen
 
 pytestmark = pytest.mark.gpu
 
@@ -136,6 +136,95 @@ def test_mat2_sizes_and_init(n):
     y = ak.ak_accumulate(dev_of("mat2", x), op="matmul", elem="mat2", init=init,
                          opts=ak.make_opts(no_neutral=True)).cpu().numpy().view(np.uint32)
     assert_exact(y.reshape(-1, 4), oracle.scan(x, "mat2", init=init))
+
+
+# --------------------------------------------------------------------------
+# long lines: the TMA tile scan (integer element types; lines of 128-byte
+# rows, tiles of 256 rows: 8192 i32 or 4096 i64; a line's last tile may be
+# partial or hold only a partial row; several lines must start on a row
+# boundary) against the super-tile scan (forced by items_per_thread), and
+# the super-tile scan on the same shapes for the other element types
+# --------------------------------------------------------------------------
+
+TMA_CASES = [("f32", 32), ("f64", 16), ("i64", 16), ("i32", 32), ("mat2", 8)]
+
+
+def _scan_both(kind, x, shape, dim, **kw):
+    """The default path and the super-tile path (forced by items_per_thread)."""
+    items = {"f32": 32, "f64": 16, "i64": 16, "i32": 32, "mat2": 8}[kind]
+    xd = dev_of(kind, x).reshape(tuple(reversed(shape)) + ((4,) if kind == "mat2" else ()))
+    extra = {"op": "matmul", "elem": "mat2"} if kind == "mat2" else {}
+    extra.update(kw)
+    opts = extra.pop("opts", None)
+    a = ak.ak_accumulate(xd, dim=dim, opts=opts, **extra)
+    o2 = ak.make_opts(items_per_thread=items, no_neutral=bool(opts is not None and opts.no_neutral))
+    b = ak.ak_accumulate(xd, dim=dim, opts=o2, **extra)
+    return a.cpu().numpy(), b.cpu().numpy()
+
+
+def _check_scan(kind, x, shape, dim, got, op="add"):
+    if kind == "mat2":
+        assert_exact(got.view(np.uint32).reshape(-1, 4), oracle.scan(x, "mat2", shape, dim))
+    elif kind == "i32":
+        assert_exact(got, oracle.scan(x, "i32", shape, dim, op=op, acc_bits=32))
+    elif kind == "i64" or op != "add":
+        assert_exact(got.astype(np.float64) if kind != "i64" else got, oracle.scan(x, kind, shape, dim, op=op))
+    else:
+        mass = _mass_lines(x.astype(np.float64), shape, dim)
+        assert_close_f32(got, oracle.scan(x, kind, shape, dim), mass, rel=F64_REL if kind == "f64" else F32_REL)
+
+
+@pytest.mark.parametrize("kind,rl", TMA_CASES)
+@pytest.mark.parametrize("rows", [256 * 3, 256 * 3 + 1, 256 * 5 + 77])
+@pytest.mark.parametrize("tail", [0, 1, 5])
+def test_tma_single_line(kind, rl, rows, tail):
+    n = rows * rl + tail
+    x = synth.mat2_modp(n, stream=80) if kind == "mat2" else gen(kind, n, stream=80)
+    a, b = _scan_both(kind, x, (n,), -1)
+    _check_scan(kind, x, (n,), -1, a)
+    _check_scan(kind, x, (n,), -1, b)
+
+
+@pytest.mark.parametrize("kind,rl", TMA_CASES)
+@pytest.mark.parametrize("rows,lines", [(256 * 2 + 5, 3), (256 * 4, 2), (300, 7)])
+def test_tma_lines_along_dim1(kind, rl, rows, lines):
+    shape = (rows * rl, lines)
+    n = rows * rl * lines
+    x = synth.mat2_modp(n, stream=81) if kind == "mat2" else gen(kind, n, stream=81)
+    a, b = _scan_both(kind, x, shape, 0)
+    _check_scan(kind, x, shape, 0, a)
+    _check_scan(kind, x, shape, 0, b)
+
+
+@pytest.mark.parametrize("op", ["max", "min", "add"])
+def test_tma_optional_partials_and_init(op):
+    n = 8192 * 6 + 40
+    x = gen("f32", n, stream=82, dist="normal")
+    opts = ak.make_opts(no_neutral=True)
+    y = ak.ak_accumulate(dev_of("f32", x), op=op, opts=opts).cpu().numpy()
+    _check_scan("f32", x, (n,), -1, y, op=op)
+    xi = gen("i64", n, stream=83)
+    y = ak.ak_accumulate(dev_of("i64", xi), op=op, init=-77, opts=opts).cpu().numpy()
+    assert_exact(y, oracle.scan(xi, "i64", op=op, init=-77))
+
+
+def test_tma_unaligned_views_fall_back():
+    n = 8192 * 4 + 3
+    x = gen("f32", n + 1, stream=84, dist="normal")
+    xd = dev_of("f32", x)[1:]
+    y = ak.ak_accumulate(xd).cpu().numpy()
+    _check_scan("f32", x[1:], (n,), -1, y)
+    out = torch.empty(n + 1, device="cuda")
+    ak.ak_accumulate(dev_of("f32", x[1:]), dst=out[1:])
+    _check_scan("f32", x[1:], (n,), -1, out[1:].cpu().numpy())
+
+
+def test_tma_in_place_ragged():
+    n = 4096 * 7 + 9
+    x = gen("i64", n, stream=85)
+    xd = dev_of("i64", x)
+    ak.ak_accumulate(xd, dst=xd, op="max")
+    assert_exact(xd.cpu().numpy(), oracle.scan(x, "i64", op="max"))
 
 
 # --------------------------------------------------------------------------
