@@ -67,11 +67,16 @@ constexpr int default_seg() {
 }
 // Predecessor super-tiles one look-back round inspects, per thread.
 constexpr int kLookSlots = 2;
-// TMA tile scan: threads per block (one 128-byte row each, so a tile is
-// kTmaBlock * 128 bytes) and tiles staged per block (the one being scanned,
-// the one folded ahead of it, and the copies in flight).
-constexpr int kTmaBlock = 256;
-constexpr int kTmaStages = 3;
+// TMA tile scan: rows of 128 bytes per tile (32 KB tiles), warp roles of
+// its one block per SM (warp 0 produces, then the look-back, fold and scan
+// warps), and look-back records read per lane per batch.
+constexpr int kWsRows = 256;
+constexpr int kWsLookWarps = 2;                                   // warps 1..2 look back
+constexpr int kWsFoldWarp0 = 1 + kWsLookWarps;                    // warps 3..10 fold
+constexpr int kWsScanWarp0 = kWsFoldWarp0 + kWsRows / 32;         // warps 11..18 scan
+constexpr int kWsThreads = (kWsScanWarp0 + kWsRows / 32) * 32;    // 608
+constexpr int kWsLookQ = 4;
+constexpr int kWsLookDefer = 1;  // a look-back also waits for this many later stages to be folded
 // Resident blocks per SM the register budget is sized for: 3 blocks of 256
 // threads (<= 80 registers a thread), a quarter of the thread slots for
 // 16-byte elements.
@@ -218,24 +223,6 @@ __device__ __forceinline__ uint64_t read_rec(const TileRec<P>* r, uint64_t epoch
     return rec_decode<P>(w, epoch, v);
 }
 
-// The records of one look-back window as raw words, read ahead of their
-// use (the loads are in flight while the block does other work) and
-// validated when they are consumed.
-template <class P, int S>
-struct LookWin {
-    uint64_t w[S][rec_words<P>()];
-};
-
-template <class P, int S>
-__device__ __forceinline__ void look_issue(LookWin<P, S>& w, const TileRec<P>* recs, int64_t base, int64_t g_first) {
-#pragma unroll
-    for (int k = 0; k < S; ++k) {
-#pragma unroll
-        for (int i = 0; i < rec_words<P>(); ++i) w.w[k][i] = 0;
-        if (base + k >= g_first) rec_load(recs + base + k, w.w[k]);
-    }
-}
-
 struct ScanCtl {
     uint64_t epoch;
     uint64_t* error_word;
@@ -283,17 +270,15 @@ __device__ __forceinline__ typename M::P block_reduce_ordered(typename M::P v, t
 // back. The window is wide enough that the published-prefix frontier keeps
 // up with the rate at which tiles start. Returns false (in every thread)
 // when a wait ran out or another block gave up.
-template <class M, int BLOCK, int SLOTS = kLookSlots, bool FAST = true>
+template <class M, int BLOCK>
 __device__ __forceinline__ bool look_back(int64_t g, int64_t g_first, const TileState<typename M::P>& ts,
                                           const ScanCtl& ctl, typename M::P* red, int* ints,
-                                          typename M::P* excl0,
-                                          const LookWin<typename M::P, SLOTS>* pre = nullptr) {
+                                          typename M::P* excl0) {
     using P = typename M::P;
-    constexpr int W = BLOCK / kWarp, S = SLOTS, WIN = S * BLOCK;
+    constexpr int W = BLOCK / kWarp, S = kLookSlots, WIN = S * BLOCK;
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
     // Fast path: warp 0 reads the 32 nearest records once; when an inclusive
     // prefix is among them and every newer one has published, that decides.
-    if constexpr (FAST) {
     if (warp == 0) {
         const int64_t idx = g - kWarp + lane;
         const bool valid = idx >= g_first;
@@ -311,7 +296,6 @@ __device__ __forceinline__ bool look_back(int64_t g, int64_t g_first, const Tile
     }
     __syncthreads();
     if (ints[2 * kWarp]) return true;
-    }
 
     P excl = M::empty();
     int64_t hi = g - 1;
@@ -320,25 +304,11 @@ __device__ __forceinline__ bool look_back(int64_t g, int64_t g_first, const Tile
         const int64_t base = hi - (WIN - 1) + (int64_t)S * tid;  // this thread's first slot
         uint64_t st[S];
         P val[S];
-        if (pre != nullptr && hi == g - 1) {
-            // the first window was read ahead: validate those words now
 #pragma unroll
-            for (int k = 0; k < S; ++k) {
-                st[k] = 0;
-                val[k] = M::empty();
-                if (base + k >= g_first) {
-                    P v;
-                    st[k] = rec_decode<P>(pre->w[k], ctl.epoch, &v);
-                    if (st[k] != 0) val[k] = v;
-                }
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < S; ++k) {
-                st[k] = 0;
-                val[k] = M::empty();
-                if (base + k >= g_first) st[k] = read_rec(ts.recs + base + k, ctl.epoch, &val[k]);
-            }
+        for (int k = 0; k < S; ++k) {
+            st[k] = 0;
+            val[k] = M::empty();
+            if (base + k >= g_first) st[k] = read_rec(ts.recs + base + k, ctl.epoch, &val[k]);
         }
         // nearest inclusive prefix seen so far: the highest window position
         int mine = -1;
@@ -750,19 +720,16 @@ __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Ac
 // TMA tile scan: one read and one write of every element
 // ---------------------------------------------------------------------------
 
-// Shared memory of one block: the staged tiles, plus slack to align them to
-// the 1024 bytes that the 128-byte swizzle pattern repeats over.
-template <int BLOCK, int STAGES>
-constexpr int tma_smem_bytes() {
-    return STAGES * BLOCK * 128 + 1024;
+// Stages of the ring and the block's dynamic shared memory: each stage
+// holds a tile and its rows' in-tile prefixes; plus slack to align the
+// tiles to the 1024 bytes that the 128-byte swizzle pattern repeats over.
+template <class P>
+constexpr int ws_stages() {
+    return sizeof(P) <= 16 ? 6 : 5;
 }
-// Resident blocks per SM the register budget is sized for (as many as the
-// staged tiles leave room for in the SM's 228 KB of shared memory).
-template <int BLOCK, int STAGES>
-constexpr int tma_min_blocks() {
-    return (228 * 1024) / (tma_smem_bytes<BLOCK, STAGES>() + 2048) < 1
-               ? 1
-               : (228 * 1024) / (tma_smem_bytes<BLOCK, STAGES>() + 2048);
+template <class P>
+constexpr int ws_smem_bytes() {
+    return ws_stages<P>() * (kWsRows * 128 + kWsRows * (int)sizeof(P)) + 1024;
 }
 
 // Row r of a swizzled tile <-> the R elements of a thread, 16 bytes at a time.
@@ -781,22 +748,6 @@ __device__ __forceinline__ void row_load(T (&run)[R], const unsigned char* buf, 
             for (int q = 0; q < WPE; ++q) e[q] = w[k * WPE + q];
             memcpy(&run[j * E + k], e, sizeof(T));
         }
-    }
-}
-template <class T, int R>
-__device__ __forceinline__ void row_store(unsigned char* buf, int r, const T (&run)[R]) {
-    constexpr int WPE = sizeof(T) / 4, E = 16 / sizeof(T);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        uint32_t w[4];
-#pragma unroll
-        for (int k = 0; k < E; ++k) {
-            uint32_t e[WPE];
-            memcpy(e, &run[j * E + k], sizeof(T));
-#pragma unroll
-            for (int q = 0; q < WPE; ++q) w[k * WPE + q] = e[q];
-        }
-        *reinterpret_cast<uint4*>(buf + swz128(r, j)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -859,230 +810,372 @@ __device__ __forceinline__ void row_scan_from(T (&run)[R], const typename M::P& 
     }
 }
 
+// Named barrier over `n` threads; returns whether `v` held in any of them.
+__device__ __forceinline__ bool group_any(bool v, int id, int n) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void group_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// Bounded wait for a ring barrier's phase; false when the wait limit passes
+// or another block gave up.
+__device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, const ScanCtl& ctl) {
+    const uint64_t t0 = globaltimer_ns();
+    for (int i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > (uint64_t)ctl.wait_limit_ns) return false;
+        if ((i & 63) == 63 && aborted(ctl)) return false;
+    }
+}
+
+__device__ __forceinline__ void give_up(const ScanCtl& ctl) {
+    atomicExch(reinterpret_cast<unsigned long long*>(ctl.error_word), (unsigned long long)ctl.epoch);
+}
+
 // Long contiguous lines, element type = accumulator type = output type,
-// viewed as rows of 128 bytes (R elements): a tile is BLOCK rows and thread
-// t owns row t. A persistent block works through the tiles it claims (in
-// claim order) with a ring of STAGES shared-memory stages: in round n it
-// scans tile n, holds tile n+1 (already folded, its aggregate published)
-// and has the copies of tiles n+2 .. n+STAGES-1 in flight. Thread 0 claims
-// tile indices from the call's counter (one claim in flight ahead of its
-// use) and has each tile copied by one bulk tensor load, swizzled so that
-// every thread reads its own row without bank conflicts.
+// viewed as rows of 128 bytes (R elements); a tile is 256 rows (32 KB). One
+// persistent block per SM runs a ring of STAGES tiles through four warp
+// roles, handing each stage on with transaction barriers in shared memory:
 //
-// Round n: refill the stage freed by round n-1 with the next claimed tile;
-// fold tile n+1 -- every thread folds its row, the row totals are scanned
-// across the block, the tile's aggregate is published (a line's first tile:
-// its inclusive prefix) and each thread keeps its exclusive in-tile prefix;
-// look back to tile n's exclusive prefix (decoupled look-back over the
-// fence-free tile records) and publish its inclusive prefix; every thread
-// reads its row of tile n again, scans it from its exclusive prefix and
-// writes it back in place; one bulk tensor store writes the tile out.
-// Because a tile's aggregate is published one round before its own look-
-// back, look-backs find their predecessors published instead of waiting on
-// them (the same deferral as the super-tile scan, with the tile held in
-// shared memory rather than in L2). HBM traffic is one read and one write of
-// every element; the operator is applied twice per element, as in any
-// single-pass scan whose tiles cannot wait for their prefix before
-// starting. Rows past a line's end are zero-filled by the copy and ignored;
-// the partial row of a single ragged line is read and written directly by
-// its thread.
-template <class T, class M, int BLOCK, int STAGES>
-__global__ void __launch_bounds__(BLOCK, (tma_min_blocks<BLOCK, STAGES>()))
+//  producer (warp 0, one thread): claims tile indices from the call's
+//    counter in order (one claim in flight ahead of its use) and, once the
+//    scan warps have released a stage, has the next tile copied into it by
+//    one bulk tensor load, swizzled so that every thread reads its own row
+//    without bank conflicts;
+//  fold warps (8): thread r folds row r, the row totals are scanned across
+//    the group, each row's exclusive in-tile prefix goes to shared memory and
+//    the tile's aggregate is published at once (the fold never waits on
+//    another block);
+//  look-back warps (kWsLookWarps, taking the stages in turn): compute each
+//    tile's exclusive prefix from the previous tile of this block -- that
+//    tile's inclusive prefix, then the aggregates of the tiles claimed in
+//    between by other blocks (about one per block, read in one batch of
+//    vector loads and folded in order). The warps fold their batches in
+//    parallel and hand the running inclusive prefix on in tile order through
+//    shared memory. Only aggregates are ever waited for, and those are
+//    published as soon as a tile lands, so no prefix has to travel from
+//    block to block and look-backs do not chain;
+//  scan warps (8): thread r reads row r again, scans it from the tile's
+//    exclusive prefix combined with the row's in-tile prefix and stores it
+//    straight to global memory, then the stage goes back to the producer.
+//
+// HBM traffic is one read and one write of every element; the operator is
+// applied twice per element (fold and scan), as in any single-pass scan
+// whose tiles cannot wait for their prefix before starting. Rows past a
+// line's end are zero-filled by the copy and ignored; the partial row of a
+// single ragged line is read and written directly by its thread. Every wait
+// is bounded and watches the call's error word; a role that gives up
+// records the call's epoch there, and the producer lets its copies land
+// before it leaves.
+template <class T, class M>
+__global__ void __launch_bounds__(kWsThreads, 1)
     k_scan_tma(const __grid_constant__ CUtensorMap tin, const T* __restrict__ x, T* __restrict__ y, int64_t len,
                int64_t rows_full, int64_t tiles_per_line, int64_t ntiles, TileState<typename M::P> ts, ScanCtl ctl,
                bool has_init, T init) {
-    static_assert(STAGES >= 3, "a stage scanned, a stage folded, at least one copy in flight");
-    constexpr int LS = 512 / BLOCK > kLookSlots ? 512 / BLOCK : kLookSlots;  // look-back window: LS * BLOCK tiles
     using P = typename M::P;
+    constexpr int S = ws_stages<P>();
     constexpr int R = 128 / (int)sizeof(T);
-    constexpr int W = BLOCK / kWarp;
-    constexpr uint32_t TILE_BYTES = BLOCK * 128;
+    constexpr int ROWS = kWsRows;
+    constexpr uint32_t TILE_BYTES = ROWS * 128;
+    constexpr int NW = rec_words<P>();
+    constexpr int Q = kWsLookQ;
     extern __shared__ unsigned char dyn_smem[];
     unsigned char* const bufs =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t full[STAGES];
-    __shared__ int64_t s_k[STAGES];
-    __shared__ P warp_tot[W];
-    __shared__ P red[W];
-    __shared__ int ints[2 * kWarp + 1];
-    __shared__ P s_bc;
+    P* const rowpre = reinterpret_cast<P*>(bufs + (size_t)S * TILE_BYTES);  // [S][ROWS]
+    __shared__ __align__(8) uint64_t full[S], folded[S], ready[S], empty[S];
+    __shared__ int64_t s_k[S];
+    __shared__ int64_t s_kprev[S];  // the block's tile before s_k[s] (-1: none)
+    __shared__ P s_agg[S];
+    __shared__ P s_pre[S];
+    __shared__ P fwt[ROWS / 32];
+    // hand-off between the look-back warps, in tile order: after ring slot
+    // s_chain - 1, the inclusive prefix of that slot's tile is s_incl;
+    // s_end is the slot of the end-of-claims sentinel once it is known
+    __shared__ P s_incl;
+    __shared__ volatile int s_chain;
+    __shared__ volatile int s_end;
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
     const int64_t rem = len - rows_full * R;  // elements of the partial last row (a single line only)
 
-    // valid elements of this thread's row of tile k
-    auto row_count = [&](int64_t k) -> int {
-        const int64_t row = (k % tiles_per_line) * BLOCK + tid;
+    auto row_count = [&](int64_t k, int r) -> int {
+        const int64_t row = (k % tiles_per_line) * ROWS + r;
         return row < rows_full ? R : (row == rows_full ? (int)rem : 0);
     };
-    auto row_src = [&](int64_t k) -> int64_t {
-        return (k / tiles_per_line) * len + ((k % tiles_per_line) * BLOCK + tid) * R;
-    };
-    // thread 0: start the copy of tile k into stage s; a tile holding only
-    // the partial row needs no copy, and a plain arrival completes the stage
-    auto issue = [&](int64_t k, int s) {
-        const int64_t row0 = (k % tiles_per_line) * BLOCK;
-        if (row0 < rows_full) {
-            mbar_arrive_expect_tx(&full[s], TILE_BYTES);
-            tma_load_3d(bufs + (size_t)s * TILE_BYTES, &tin, 0, (int)row0, (int)(k / tiles_per_line), &full[s]);
-        } else {
-            mbar_arrive(&full[s]);
-        }
-    };
-    // thread 0, after a failure: let the copies of ring slots first..last
-    // that were started land before the block leaves (each wait bounded)
-    auto drain = [&](int first, int last) {
-        const uint64_t until = globaltimer_ns() + (uint64_t)ctl.wait_limit_ns;
-        for (int j = first; j <= last; ++j) {
-            const int s = j % STAGES;
-            if (s_k[s] < ntiles) mbar_wait(&full[s], (uint32_t)(j / STAGES) & 1u, until);
-        }
-    };
-    auto give_up = [&](int first, int last) {
-        if (tid == 0) {
-            atomicExch(reinterpret_cast<unsigned long long*>(ctl.error_word), (unsigned long long)ctl.epoch);
-            drain(first, last);
-        }
-    };
-    // every thread: wait for ring slot j's copy (bounded); false in all
-    // threads when any thread's wait ran out
-    auto landed = [&](int j) -> bool {
-        const bool ok = mbar_wait(&full[j % STAGES], (uint32_t)(j / STAGES) & 1u,
-                                  globaltimer_ns() + (uint64_t)ctl.wait_limit_ns);
-        return !__syncthreads_or(!ok);
-    };
-    // every thread: fold its row of tile k (ring slot j) and scan the row
-    // totals across the block; returns the thread's exclusive prefix within
-    // the tile, and in thread 0 *agg = the tile's aggregate, which it
-    // publishes (the first tile of a line: as its inclusive prefix)
-    auto fold_tile = [&](int64_t k, int j, P* agg) -> P {
-        const int nt = row_count(k);
-        P tot = M::empty();
-        if (nt == R) {
-            T run[R];
-            row_load(run, bufs + (size_t)(j % STAGES) * TILE_BYTES, tid);
-            tot = M::lift(row_fold<M>(run));
-        } else if (nt > 0) {
-            const T* src = x + row_src(k);
-            for (int i = 0; i < nt; ++i) tot = M::combine(tot, M::lift(src[i]));
-        }
-        const P inc = warp_inclusive_scan<M>(tot, lane);
-        P lane_excl = shfl_up_any(inc, 1);
-        if (lane == 0) lane_excl = M::empty();
-        if (lane == kWarp - 1) warp_tot[warp] = inc;
-        __syncthreads();
-        if (warp == 0) {
-            const P w = lane < W ? warp_tot[lane] : M::empty();
-            const P wi = warp_inclusive_scan<M>(w, lane);
-            P we = shfl_up_any(wi, 1);
-            if (lane == 0) we = M::empty();
-            if (lane < W) warp_tot[lane] = we;
-            const P a = shfl_idx_any(wi, W - 1);
-            if (lane == 0) *agg = a;
-        }
-        __syncthreads();
-        const P mine = M::combine(warp_tot[warp], lane_excl);
-        if (tid == 0) {
-            const int64_t t = k % tiles_per_line;
-            if (tiles_per_line > 1 && t != tiles_per_line - 1 && k != ctl.skip_tile) {
-                if (t == 0) publish(ts, k, kStatusPrefix, M::combine(has_init ? M::lift(init) : M::empty(), *agg), ctl.epoch);
-                else publish(ts, k, kStatusAggregate, *agg, ctl.epoch);
-            }
-        }
-        __syncthreads();  // warp_tot is reused by the next fold
-        return mine;
+    auto row_off = [&](int64_t k, int r) -> int64_t {
+        return (k / tiles_per_line) * len + ((k % tiles_per_line) * ROWS + r) * R;
     };
 
-    unsigned long long next_claim = 0;
     if (tid == 0) {
 #pragma unroll
-        for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
-        fence_barrier_init();
-        tma_prefetch_map(&tin);
-        for (int s = 0; s < STAGES - 1; ++s) {
-            const int64_t k = claim_tile(ctl, ntiles);
-            s_k[s] = k;
-            if (k < ntiles) issue(k, s);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&folded[s], 1);
+            mbar_init(&ready[s], 1);
+            mbar_init(&empty[s], ROWS / 32);
         }
-        next_claim = atomicAdd(ctl.counter, 1ull);
+        fence_barrier_init();
+        s_chain = 0;
+        s_end = 1 << 30;
     }
     __syncthreads();
-    if (s_k[0] >= ntiles) return;  // claims only grow: nothing was started
-    if (!landed(0)) {
-        give_up(0, STAGES - 2);
+
+    if (warp == 0) {
+        // ---------------- producer
+        if (lane != 0) return;
+        tma_prefetch_map(&tin);
+        unsigned long long next = atomicAdd(ctl.counter, 1ull);
+        int64_t kprev = -1;
+        int j = 0;
+        for (;; ++j) {
+            const int s = j % S;
+            if (j >= S && !ring_wait(&empty[s], (uint32_t)(j / S - 1) & 1u, ctl)) {
+                give_up(ctl);
+                break;
+            }
+            const int64_t k = (int64_t)next;
+            s_k[s] = k;
+            s_kprev[s] = kprev;
+            kprev = k;
+            if (k >= ntiles) {  // end of the claims: pass the sentinel down the ring
+                mbar_arrive(&full[s]);
+                ++j;
+                break;
+            }
+            next = atomicAdd(ctl.counter, 1ull);
+            const int64_t row0 = (k % tiles_per_line) * ROWS;
+            if (row0 < rows_full) {
+                mbar_arrive_expect_tx(&full[s], TILE_BYTES);
+                tma_load_3d(bufs + (size_t)s * TILE_BYTES, &tin, 0, (int)row0, (int)(k / tiles_per_line), &full[s]);
+            } else {
+                mbar_arrive(&full[s]);  // only the partial row: nothing to copy
+            }
+        }
+        // the block's shared memory must outlive every copy started into it
+        const uint64_t until = globaltimer_ns() + (uint64_t)ctl.wait_limit_ns;
+        for (int q = (j > S ? j - S : 0); q < j; ++q) mbar_wait(&full[q % S], (uint32_t)(q / S) & 1u, until);
         return;
     }
-    P agg = M::empty();  // meaningful in thread 0
-    P mine = fold_tile(s_k[0], 0, &agg);
-    const uint64_t last_use = l2_policy_evict_first();
 
-    for (int n = 0;; ++n) {
-        const int b = n % STAGES;
-        const int64_t k = s_k[b];
-        if (tid == 0) {
-            // refill the stage freed by the previous round with the next claimed tile
-            const int bl = (n + STAGES - 1) % STAGES;
-            const int64_t kn = (int64_t)next_claim;
-            next_claim = atomicAdd(ctl.counter, 1ull);
-            s_k[bl] = kn;
-            if (kn < ntiles) issue(kn, bl);
-        }
-        // read tile k's look-back window now; the fold below hides the latency
-        const int64_t t = k % tiles_per_line;
-        LookWin<P, LS> win;
-        if (t != 0) look_issue(win, ts.recs, (k - 1) - (LS * BLOCK - 1) + (int64_t)LS * tid, k - t);
-
-        // fold the next tile: its aggregate goes out a round before its look-back
-        const int64_t k1 = s_k[(n + 1) % STAGES];
-        P agg1 = M::empty();
-        P mine1 = M::empty();
-        if (k1 < ntiles) {
-            if (!landed(n + 1)) {
-                give_up(n + 1, n + STAGES - 1);
+    if (warp <= kWsLookWarps) {
+        // ---------------- look-back (this warp takes ring slots lw, lw + L, ...)
+        const int lw = warp - 1;
+        for (int j = lw;; j += kWsLookWarps) {
+            const int s = j % S;
+            bool ok = true;
+            {
+                const uint64_t t0 = globaltimer_ns();
+                for (int i = 0;; ++i) {
+                    if (mbar_try_wait(&folded[s], (uint32_t)(j / S) & 1u)) break;
+                    if (s_end < j) return;  // the claims ended in an earlier slot
+                    if (globaltimer_ns() - t0 > (uint64_t)ctl.wait_limit_ns || ((i & 63) == 63 && aborted(ctl))) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (__any_sync(kFull, !ok)) {
+                if (lane == 0) give_up(ctl);
                 return;
             }
-            mine1 = fold_tile(k1, n + 1, &agg1);
+            const int64_t k = s_k[s];
+            if (k >= ntiles) {
+                if (lane == 0) {
+                    s_end = j;
+                    mbar_arrive(&ready[s]);
+                }
+                return;
+            }
+            // Give the other blocks time to publish the tiles they claimed
+            // just before this one: wait until the next kWsLookDefer stages
+            // of this block are folded too (their copies were started after
+            // this tile's, so by then the in-between tiles have landed
+            // elsewhere as well). A stage past the end of the claims is
+            // folded as a sentinel; the ring is deep enough that this never
+            // waits on a stage that needs this look-back to make progress.
+            for (int d = 1; d <= kWsLookDefer && ok; ++d) {
+                const int jd = j + d, sd = jd % S;
+                const uint64_t t0 = globaltimer_ns();
+                for (int i = 0;; ++i) {
+                    if (mbar_try_wait(&folded[sd], (uint32_t)(jd / S) & 1u)) break;
+                    if (globaltimer_ns() - t0 > (uint64_t)ctl.wait_limit_ns || ((i & 63) == 63 && aborted(ctl))) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (s_k[sd] >= ntiles) break;  // the sentinel: nothing after it
+            }
+            if (__any_sync(kFull, !ok)) {
+                if (lane == 0) give_up(ctl);
+                return;
+            }
+            const int64_t t = k % tiles_per_line, first = k - t, kp = s_kprev[s];
+            const bool chained = t != 0 && kp >= first;  // prefix continues from the block's previous tile
+            const int64_t lo = t == 0 ? k : (chained ? kp + 1 : first);
+            // fold the aggregates of tiles lo .. k-1 in order
+            P f = M::empty();
+            bool good = true;
+            for (int64_t base = lo; base < k; base += (int64_t)kWarp * Q) {
+                const int64_t mine = base + (int64_t)lane * Q;  // this lane's Q consecutive tiles
+                uint64_t w[Q][NW];
+#pragma unroll
+                for (int q = 0; q < Q; ++q)
+                    if (mine + q < k) rec_load(ts.recs + mine + q, w[q]);
+                P vals[Q];
+                unsigned pend = 0;  // records of this lane not published yet
+#pragma unroll
+                for (int q = 0; q < Q; ++q) {
+                    vals[q] = M::empty();
+                    if (mine + q < k && rec_decode<P>(w[q], ctl.epoch, &vals[q]) == 0) pend |= 1u << q;
+                }
+                const uint64_t t0 = globaltimer_ns();
+                while (pend != 0) {  // read every pending record again, all at once
+                    if (globaltimer_ns() - t0 > (uint64_t)ctl.wait_limit_ns || aborted(ctl)) {
+                        good = false;
+                        break;
+                    }
+                    __nanosleep(100);
+#pragma unroll
+                    for (int q = 0; q < Q; ++q)
+                        if (pend & (1u << q)) rec_load(ts.recs + mine + q, w[q]);
+#pragma unroll
+                    for (int q = 0; q < Q; ++q)
+                        if ((pend & (1u << q)) && rec_decode<P>(w[q], ctl.epoch, &vals[q]) != 0) pend &= ~(1u << q);
+                }
+                P v = M::empty();
+#pragma unroll
+                for (int q = 0; q < Q; ++q)
+                    if (mine + q < k) v = M::combine(v, vals[q]);
+                if (__any_sync(kFull, !good)) {
+                    good = false;
+                    break;
+                }
+                v = warp_reduce<M>(v);  // lane 0 holds the ordered fold of the batch
+                f = M::combine(f, shfl_idx_any(v, 0));
+            }
+            if (!good) {
+                if (lane == 0) give_up(ctl);
+                return;
+            }
+            // wait for this slot's turn in the hand-off
+            {
+                const uint64_t t0 = globaltimer_ns();
+                for (int i = 0; s_chain != j; ++i) {
+                    if (globaltimer_ns() - t0 > (uint64_t)ctl.wait_limit_ns || ((i & 63) == 63 && aborted(ctl))) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (__any_sync(kFull, !ok)) {
+                if (lane == 0) give_up(ctl);
+                return;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                const P start = chained ? s_incl : (has_init ? M::lift(init) : M::empty());
+                const P excl = M::combine(start, f);
+                s_pre[s] = excl;
+                s_incl = M::combine(excl, s_agg[s]);
+                __threadfence_block();
+                s_chain = j + 1;
+                mbar_arrive(&ready[s]);
+            }
+            __syncwarp();
         }
+    }
 
-        // tile k's exclusive prefix
-        P prefix = has_init ? M::lift(init) : M::empty();
-        if (t != 0) {
-            if (!look_back<M, BLOCK, LS, false>(k, k - t, ts, ctl, red, ints, &prefix, &win)) {
-                give_up(n + 2, n + STAGES - 1);
-                return;  // uniform: every thread got the same answer
+    if (warp < kWsScanWarp0) {
+        // ---------------- fold
+        const int r = tid - kWsFoldWarp0 * kWarp, fw = r / kWarp;
+        for (int j = 0;; ++j) {
+            const int s = j % S;
+            const bool ok = ring_wait(&full[s], (uint32_t)(j / S) & 1u, ctl);
+            if (group_any(!ok, 1, ROWS)) {
+                if (r == 0) give_up(ctl);
+                return;
             }
-            if (tid == 0) {
-                if (t != tiles_per_line - 1 && k != ctl.skip_tile)
-                    publish(ts, k, kStatusPrefix, M::combine(prefix, agg), ctl.epoch);
-                s_bc = prefix;
+            const int64_t k = s_k[s];
+            if (k >= ntiles) {
+                if (r == 0) mbar_arrive(&folded[s]);
+                return;
             }
-            __syncthreads();
-            prefix = s_bc;
+            const int nt = row_count(k, r);
+            P tot = M::empty();
+            if (nt == R) {
+                T run[R];
+                row_load(run, bufs + (size_t)s * TILE_BYTES, r);
+                tot = M::lift(row_fold<M>(run));
+            } else if (nt > 0) {
+                const T* src = x + row_off(k, r);
+                for (int i = 0; i < nt; ++i) tot = M::combine(tot, M::lift(src[i]));
+            }
+            const P inc = warp_inclusive_scan<M>(tot, lane);
+            P lane_excl = shfl_up_any(inc, 1);
+            if (lane == 0) lane_excl = M::empty();
+            if (lane == kWarp - 1) fwt[fw] = inc;
+            group_sync(1, ROWS);
+            if (fw == 0) {
+                const P wv = lane < ROWS / 32 ? fwt[lane] : M::empty();
+                const P wi = warp_inclusive_scan<M>(wv, lane);
+                P we = shfl_up_any(wi, 1);
+                if (lane == 0) we = M::empty();
+                const P agg = shfl_idx_any(wi, ROWS / 32 - 1);
+                if (lane < ROWS / 32) fwt[lane] = we;
+                if (lane == 0) {
+                    s_agg[s] = agg;
+                    const int64_t t = k % tiles_per_line;
+                    if (t != tiles_per_line - 1 && k != ctl.skip_tile) publish(ts, k, kStatusAggregate, agg, ctl.epoch);
+                }
+            }
+            group_sync(1, ROWS);
+            rowpre[(size_t)s * ROWS + r] = M::combine(fwt[fw], lane_excl);
+            group_sync(1, ROWS);  // every row prefix written; fwt free again
+            if (r == 0) mbar_arrive(&folded[s]);
         }
+    }
 
-        // scan the row from the thread's exclusive prefix and store it
-        unsigned char* const buf = bufs + (size_t)b * TILE_BYTES;
-        const int nt = row_count(k);
-        const P from = M::combine(prefix, mine);
-        if (nt == R) {
-            T run[R];
-            row_load(run, buf, tid);
-            row_scan_from<M>(run, from);
-            row_store_global(y + row_src(k), run, last_use);
-        } else if (nt > 0) {
-            const T* src = x + row_src(k);
-            T* dst = y + row_src(k);
-            P a = from;
-            for (int i = 0; i < nt; ++i) {
-                a = M::combine(a, M::lift(src[i]));
-                dst[i] = M::value(a);
+    {
+        // ---------------- scan
+        const int r = tid - kWsScanWarp0 * kWarp;
+        const uint64_t last_use = l2_policy_evict_first();
+        for (int j = 0;; ++j) {
+            const int s = j % S;
+            const bool ok = ring_wait(&ready[s], (uint32_t)(j / S) & 1u, ctl);
+            if (__any_sync(kFull, !ok)) {
+                if (lane == 0) give_up(ctl);
+                return;
             }
+            const int64_t k = s_k[s];
+            if (k >= ntiles) return;
+            const P from = M::combine(s_pre[s], rowpre[(size_t)s * ROWS + r]);
+            const int nt = row_count(k, r);
+            if (nt == R) {
+                T run[R];
+                row_load(run, bufs + (size_t)s * TILE_BYTES, r);
+                row_scan_from<M>(run, from);
+                row_store_global(y + row_off(k, r), run, last_use);
+            } else if (nt > 0) {
+                const T* src = x + row_off(k, r);
+                T* dst = y + row_off(k, r);
+                P a = from;
+                for (int i = 0; i < nt; ++i) {
+                    a = M::combine(a, M::lift(src[i]));
+                    dst[i] = M::value(a);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
         }
-        // the stage is refilled next round: every thread is done reading it
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (k1 >= ntiles) break;  // claims only grow: nothing further was started
-        agg = agg1;
-        mine = mine1;
     }
 }
 
@@ -1172,15 +1265,15 @@ bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const 
 template <class T, class M>
 int tma_blocks_per_sm(int device) {
     static std::atomic<int> cache[64];
-    auto kernel = k_scan_tma<T, M, kTmaBlock, kTmaStages>;
-    constexpr int smem = tma_smem_bytes<kTmaBlock, kTmaStages>();
+    auto kernel = k_scan_tma<T, M>;
+    constexpr int smem = ws_smem_bytes<typename M::P>();
     if (device >= 0 && device < 64) {
         const int v = cache[device].load(std::memory_order_relaxed);
         if (v > 0) return v;
     }
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kTmaBlock, smem) != cudaSuccess) return -1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kWsThreads, smem) != cudaSuccess) return -1;
     if (occ < 1) return 0;
     if (device >= 0 && device < 64) cache[device].store(occ, std::memory_order_relaxed);
     return occ;
@@ -1198,7 +1291,7 @@ ak_status launch_tma(const ScanCall& c, const ScanPlan& p) {
     const int64_t rows_full = c.len / R;
     const uint64_t line_bytes = c.outer > 1 ? (uint64_t)c.len * sizeof(T) : (uint64_t)rows_full * 128;
     alignas(64) CUtensorMap tin;
-    if (!encode_rows(enc, &tin, c.src, rows_full, c.outer, line_bytes, kTmaBlock)) return AK_ERR_UNSUPPORTED;
+    if (!encode_rows(enc, &tin, c.src, rows_full, c.outer, line_bytes, kWsRows)) return AK_ERR_UNSUPPORTED;
     DeviceInfo dev;
     if (!current_device(&dev)) return AK_ERR_CUDA;
     const int occ = tma_blocks_per_sm<T, M>(dev.device);
@@ -1220,11 +1313,9 @@ ak_status launch_tma(const ScanCall& c, const ScanPlan& p) {
     // fresh counter, error word and records (correct under CUDA graph replay)
     cudaError_t e = cudaMemsetAsync(ws, 0, p.tma_ws_bytes, c.stream);
     if (e != cudaSuccess) return cuda_fail(e);
-    k_scan_tma<T, M, kTmaBlock, kTmaStages><<<(unsigned)grid, kTmaBlock, tma_smem_bytes<kTmaBlock, kTmaStages>(),
-                                               c.stream>>>(tin, static_cast<const T*>(c.src),
-                                                           static_cast<T*>(c.dst), c.len, rows_full,
-                                                           p.tma_tiles_per_line, p.tma_tiles, ts, ctl, c.has_init,
-                                                           init);
+    k_scan_tma<T, M><<<(unsigned)grid, kWsThreads, ws_smem_bytes<typename M::P>(), c.stream>>>(
+        tin, static_cast<const T*>(c.src), static_cast<T*>(c.dst), c.len, rows_full, p.tma_tiles_per_line,
+        p.tma_tiles, ts, ctl, c.has_init, init);
     ak_status s = check_launch();
     if (s == AK_OK) count_launches(1);
     return s;
@@ -1253,7 +1344,8 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
     } else {
         if (p.block != BLOCK || p.items != ITEMS) return AK_ERR_UNSUPPORTED;
         if constexpr (std::is_same_v<In, Acc> && std::is_same_v<Acc, Out> &&
-                      (sizeof(Acc) == 4 || sizeof(Acc) == 8 || sizeof(Acc) == 16)) {
+                      (std::is_same_v<Acc, float> || std::is_same_v<Acc, int32_t> || std::is_same_v<Acc, int64_t>) &&
+                      std::is_same_v<typename M::P, Acc>) {
             if (p.kind == 0 && p.tma) {
                 const ak_status st = launch_tma<Acc, M>(c, p);
                 if (st != AK_ERR_UNSUPPORTED) return st;
@@ -1346,16 +1438,19 @@ ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_d
     p->tiles_per_line = (len + super - 1) / super;
     p->tiles = p->tiles_per_line * outer;
     p->ws_bytes = align_up(kWsHeader + (size_t)p->tiles * (16 + align_up(psz, 16)), 256);  // TileRec per super-tile
-    // TMA tile scan: one integer element type (the floating-point and matrix
-    // scans do more operator work per byte and run faster as super-tiles),
-    // rows of 128 bytes, several tiles per line, and lines that start on a
-    // row boundary unless there is only one
+    // TMA tile scan: one element type throughout, f32 / i32 / i64 with a
+    // neutral element (f64 and the matrix product spend more operator work
+    // per byte, Optional partials more per combine: those run faster as
+    // super-tiles, whose blocks carry more warps per SM), rows of 128 bytes,
+    // several tiles per line, and lines that start on a row boundary unless
+    // there is only one
     const int64_t rl = 128 / (int64_t)asz;
-    if (items == 0 && in == acc && out == acc && (acc == AK_I32 || acc == AK_I64) && len > kTmaBlock * rl &&
+    if (items == 0 && in == acc && out == acc && (acc == AK_F32 || acc == AK_I32 || acc == AK_I64) && !no_neutral &&
+        len > kWsRows * rl &&
         (outer == 1 || len % rl == 0) && len / rl < ((int64_t)1 << 31) && outer < ((int64_t)1 << 31)) {
         const int64_t rows = (len + rl - 1) / rl;
         p->tma = true;
-        p->tma_tiles_per_line = (rows + kTmaBlock - 1) / kTmaBlock;
+        p->tma_tiles_per_line = (rows + kWsRows - 1) / kWsRows;
         p->tma_tiles = p->tma_tiles_per_line * outer;
         p->tma_ws_bytes = align_up(kWsHeader + (size_t)p->tma_tiles * (16 + align_up(psz, 16)), 256);
         p->ws_bytes = std::max(p->ws_bytes, p->tma_ws_bytes);
