@@ -201,10 +201,14 @@ ak_status ak_reduce_dims(const void* src, int ndim, const int64_t* shape, uint32
  *   y_1 = op(init, x_1) (or x_1 without init), y_i = op(y_{i-1}, x_i).
  * dim = -1 scans the whole array as one line (column-major order); dim = d
  * scans every line along dimension d independently. PR #202, first
- * paragraph: a tile is loaded striped, each thread scans its own run of
- * consecutive elements, and the tile prefix is applied; runs are stored at an
- * odd stride in shared memory. Tiles pass their prefixes on in a single pass
- * (decoupled look-back, Merrill & Garland 2016); every wait is bounded.
+ * paragraph: a tile is loaded, each thread scans its own run of consecutive
+ * elements, and the tile prefix is applied (runs of lines that fit one tile
+ * sit at an odd stride in shared memory, as there; long lines are copied by
+ * the TMA engine into a swizzled ring, or walked in 32-byte segments). Tiles
+ * pass their prefixes on in a single pass from published tile aggregates
+ * (after decoupled look-back, Merrill & Garland 2016); every wait is bounded.
+ * Long-line calls clear their own tile state on `stream` first, so a call
+ * captured in a CUDA graph is correct on every replay.
  *
  *   src, dst      device, same shape; dst may equal src (in place) but must
  *                 not otherwise overlap it
