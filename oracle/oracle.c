@@ -127,7 +127,9 @@ static void ffold_step(ffold* a, double v, int op) {
     }
 }
 
-static double ffold_value(const ffold* a) { return isfinite(a->s) ? a->s + a->c : a->s; }
+/* The compensated value; with no compensation the running value itself, so
+ * a fold of negative zeros stays -0.0 (s + 0.0 would turn it into +0.0). */
+static double ffold_value(const ffold* a) { return (isfinite(a->s) && a->c != 0.0) ? a->s + a->c : a->s; }
 
 /* ------------------------------------------------------------------------ */
 /* integer fold: exact, wrapped to 32 or 64 bits                           */

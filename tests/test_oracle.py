@@ -419,3 +419,17 @@ def test_synth_is_deterministic_and_on_grid():
     assert np.array_equal(w[40:60], synth.words(20, stream=5, offset=40))
     i = synth.uniform_int(10_000, -1000, 1000, np.int32)
     assert i.min() == -1000 and i.max() == 1000
+
+
+def test_signed_zero_follows_the_left_fold():
+    # IEEE addition: -0 + -0 = -0 and -0 + +0 = +0; the left fold (and every
+    # prefix of it) keeps those signs, for sums and scans in f64 and f32 inputs
+    for kind, dt in (("f64", np.float64), ("f32", np.float32)):
+        x = np.full(7, -0.0, dtype=dt)
+        assert np.signbit(oracle.reduce(x, kind))
+        assert np.all(np.signbit(oracle.scan(x, kind)))
+        y = oracle.scan(np.array([-0.0, 0.0, -0.0], dtype=dt), kind)
+        assert list(np.signbit(y)) == [True, False, False]
+    # with an init of -0.0 the fold of -0.0 stays -0.0; a +0.0 init makes it +0.0
+    assert np.signbit(oracle.reduce(np.full(3, -0.0), "f64", init=-0.0))
+    assert not np.signbit(oracle.reduce(np.full(3, -0.0), "f64", init=0.0))
