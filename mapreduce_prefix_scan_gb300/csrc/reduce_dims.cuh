@@ -36,7 +36,7 @@ namespace ak {
 namespace dims {
 
 constexpr int kBlock = 256;
-constexpr int kUnroll = 4;          // rows in flight per thread
+constexpr int kUnroll = 8;          // rows in flight per thread
 constexpr int kMinRowsPerGroup = 8; // the selector splits no further than this many rows per group
 
 template <class Acc, class Out, class M>

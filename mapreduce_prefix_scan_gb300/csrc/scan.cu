@@ -57,13 +57,15 @@ template <class Acc>
 constexpr int default_block() {
     return sizeof(Acc) >= 16 ? 128 : 256;
 }
-// Elements of one thread's segment in the long-line scan: 256 bytes of
-// 4-byte elements (64 KB super-tiles), 512 bytes of 8-byte ones and 1 KB of
+// Elements of one thread's segment in the long-line scan: 128 bytes of
+// 4-byte accumulators (32 KB super-tiles: the 4-byte types left on this path
+// carry Optional partials, whose scans are short enough that more, smaller
+// super-tiles keep every block busy), 512 bytes of 8-byte ones and 1 KB of
 // 16-byte ones (128 KB super-tiles: more operator work per byte, so more
 // bytes per look-back).
 template <class Acc>
 constexpr int default_seg() {
-    return sizeof(Acc) >= 16 ? 64 : (sizeof(Acc) == 8 ? 64 : 64);
+    return sizeof(Acc) >= 16 ? 64 : (sizeof(Acc) == 8 ? 64 : 32);
 }
 // Predecessor super-tiles one look-back round inspects, per thread.
 constexpr int kLookSlots = 2;
@@ -506,6 +508,46 @@ __host__ __device__ constexpr int chunk_elems() {
     return 32 / (int)sizeof(In);
 }
 
+// Sum of a row of doubles in 64-bit fixed point, off the FP64 pipe (GB300
+// issues two FP64 additions per clock per SM, so a scan that adds every
+// element twice in FP64 is bound by that pipe, not by HBM). Every element is
+// aligned to the row's largest exponent with 6 guard bits below that
+// element's last mantissa bit (16 aligned values of at most 59 bits cannot
+// overflow 63 bits), negated by its sign and added exactly; bits shifted out
+// are truncated, an error below 16 * 2^-6 units in the last place of the
+// largest element, far inside the f64 scan tolerance. The integer sum is
+// rounded to double once. Rows holding an infinity or NaN (exponent field all
+// ones) or only zeros and subnormals (field all zeros) take the plain FP64
+// fold, which keeps IEEE specials and the sign of zero exact.
+template <int R>
+__device__ __forceinline__ double row_sum_fixed(const double (&run)[R]) {
+    uint32_t e[R];
+    uint32_t emax = 0;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        e[i] = ((uint32_t)__double2hiint(run[i]) >> 20) & 0x7FFu;
+        emax = max(emax, e[i]);
+    }
+    if (emax == 0x7FFu || emax == 0u) {
+        double a = run[0];
+#pragma unroll
+        for (int i = 1; i < R; ++i) a += run[i];
+        return a;
+    }
+    int64_t sum = 0;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const uint64_t bits = (uint64_t)__double_as_longlong(run[i]);
+        const uint64_t m = (bits & 0x000FFFFFFFFFFFFFull) | (e[i] != 0u ? (1ull << 52) : 0ull);
+        const uint32_t sh = emax - max(e[i], 1u);
+        const int64_t q = sh >= 64u ? 0 : (int64_t)((m << 6) >> sh);
+        sum += (bits >> 63) ? -q : q;
+    }
+    // sum * 2^(emax - 1075 - 6): one rounding in the conversion, the scaling by
+    // a power of two is exact unless the result is subnormal
+    return scalbn((double)sum, (int)emax - 1081);
+}
+
 // Fold of one segment (n <= SEG valid elements) in element order.
 template <class In, class M, int SEG>
 __device__ __forceinline__ typename M::P segment_fold(const In* src, int n, uint64_t policy) {
@@ -516,7 +558,27 @@ __device__ __forceinline__ typename M::P segment_fold(const In* src, int n, uint
     constexpr int U = NC < 8 ? NC : 8;
     static_assert(SEG % CH == 0 && NC % U == 0, "whole chunks per segment");
     if (n == SEG && reinterpret_cast<uintptr_t>(src) % 32 == 0) {
-        if constexpr (M::commutative) {
+        if constexpr (std::is_same_v<In, double> && std::is_same_v<typename M::P, double> &&
+                      std::is_same_v<typename M::op, OpAdd> && SEG % 16 == 0 && 16 % CH == 0) {
+            // groups of 16 summed in fixed point, the group sums added in FP64
+            // (16 elements = 4 loads in flight at a time: room for the integer work)
+            P a = M::empty();
+            constexpr int U4 = 16 / CH;
+#pragma unroll 1
+            for (int c0 = 0; c0 < NC; c0 += U4) {
+                Raw<32> r[U4];
+#pragma unroll
+                for (int u = 0; u < U4; ++u) r[u] = ld_hint32(src + (c0 + u) * CH, policy);
+#pragma unroll
+                for (int g = 0; g < U4 * CH / 16; ++g) {
+                    double grp[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) grp[e] = raw_get<double>(r[(g * 16 + e) / CH], (g * 16 + e) % CH);
+                    a += row_sum_fixed(grp);
+                }
+            }
+            return a;
+        } else if constexpr (M::commutative) {
             // one accumulator per chunk position: short dependency chains
             P acc[CH];
 #pragma unroll
@@ -1425,7 +1487,7 @@ ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_d
     if (items != 0 && items != it) return AK_ERR_UNSUPPORTED;
     p->items = it;
     const int block = asz >= 16 ? 128 : 256;
-    const int seg = asz >= 16 ? 64 : (asz == 8 ? 64 : 64);
+    const int seg = asz >= 16 ? 64 : (asz == 8 ? 64 : 32);
     p->block = block;
     const int64_t tile = (int64_t)block * it;
     if (len <= tile) {
@@ -1439,9 +1501,10 @@ ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_d
     p->tiles = p->tiles_per_line * outer;
     p->ws_bytes = align_up(kWsHeader + (size_t)p->tiles * (16 + align_up(psz, 16)), 256);  // TileRec per super-tile
     // TMA tile scan: one element type throughout, f32 / i32 / i64 with a
-    // neutral element (f64 and the matrix product spend more operator work
-    // per byte, Optional partials more per combine: those run faster as
-    // super-tiles, whose blocks carry more warps per SM), rows of 128 bytes,
+    // neutral element (f64 additions run on the FP64 pipe, the matrix product
+    // spends more operator work per byte, Optional partials more per combine:
+    // those run faster as super-tiles, whose blocks carry more warps per SM),
+    // rows of 128 bytes,
     // several tiles per line, and lines that start on a row boundary unless
     // there is only one
     const int64_t rl = 128 / (int64_t)asz;

@@ -208,6 +208,28 @@ def test_tma_optional_partials_and_init(op):
     assert_exact(y, oracle.scan(xi, "i64", op=op, init=-77))
 
 
+def test_f64_scan_special_values():
+    # the long-line f64 scan folds rows in 64-bit fixed point; rows of only
+    # zeros / subnormals and rows with an infinity take the plain f64 fold
+    n = 4096 * 9 + 7
+    z = np.full(n, -0.0)
+    y = ak.ak_accumulate(dev_of("f64", z)).cpu().numpy()
+    assert np.all(y == 0) and np.all(np.signbit(y))  # every prefix of -0.0 is -0.0
+    k = synth.uniform_int(n, -1000, 1000, np.int64, stream=86)
+    x = np.ldexp(synth.normal_f64(n, stream=87), k)  # exponents over the whole range
+    x[5000:5100] = 0.0
+    x[6016:6032] = 4.9e-322 * np.arange(1, 17)  # a row of subnormals only
+    x[20000:20016] = -0.0
+    want = oracle.scan(x, "f64")
+    for opts in (None, ak.make_opts(items_per_thread=16)):
+        y = ak.ak_accumulate(dev_of("f64", x), opts=opts).cpu().numpy()
+        assert_close_f32(y, want, np.cumsum(np.abs(x)), rel=F64_REL)
+    x[n - 100] = np.inf
+    y = ak.ak_accumulate(dev_of("f64", x)).cpu().numpy()
+    assert np.all(np.isfinite(y[: n - 100])) and np.all(y[n - 100:] == np.inf)
+    assert_close_f32(y[: n - 100], want[: n - 100], np.cumsum(np.abs(x[: n - 100])), rel=F64_REL)
+
+
 def test_tma_unaligned_views_fall_back():
     n = 8192 * 4 + 3
     x = gen("f32", n + 1, stream=84, dist="normal")
