@@ -80,11 +80,12 @@ constexpr int kWsThreads = (kWsScanWarp0 + kWsRows / 32) * 32;    // 608
 constexpr int kWsLookQ = 4;
 constexpr int kWsLookDefer = 1;  // a look-back also waits for this many later stages to be folded
 // Resident blocks per SM the register budget is sized for: 3 blocks of 256
-// threads (<= 80 registers a thread), a quarter of the thread slots for
-// 16-byte elements.
+// threads (<= 80 registers a thread); 5 blocks of 128 for 16-byte elements
+// (<= 96 registers: the matrix product's chains of dependent products need
+// the extra warps to hide their latency more than they need registers).
 template <int BLOCK, int ACC_BYTES>
 constexpr int min_blocks_per_sm() {
-    return ACC_BYTES >= 16 ? 2048 / BLOCK / 4 : 3;
+    return ACC_BYTES >= 16 ? 5 : 3;
 }
 
 // Shared-memory run layout: run r starts at 16-byte chunk r * run_stride.
