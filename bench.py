@@ -47,6 +47,25 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's value (the slowest rank's time), through
+    the default process group; the value itself with one process."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_value(world: int, bytes_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job throughput in GB/s: the bytes every rank moved over the
+    slowest rank's time (weak scaling: each rank runs the full workload)."""
+    return world * bytes_per_step * steps / (ms * 1e-3) / 1e9
+
+
 def _rank_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
         int(os.environ.get("LOCAL_RANK", "0"))
@@ -365,16 +384,13 @@ def run_ours(args):
     launches = ak.ak_kernel_launch_count() - launches0
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = _max_over_ranks(ms, dev)
     per_call_us = {}
     for k, (name, _, _) in enumerate(calls):
         per_call_us[name] = statistics.median([evs[i][k][0].elapsed_time(evs[i][k][1]) * 1e3 for i in range(args.steps)])
     call_us_total = sum(per_call_us[c[0]] for c in calls)
     achieved = step_bytes / call_us_total / 1e3  # GB/s over the ak_reduce calls
-    value = world * step_bytes * args.steps / (ms * 1e-3) / 1e9
+    value = _job_value(world, step_bytes, args.steps, ms)
 
     # end to end: host buffers, H2D inside the timed region, D2H of the results
     e2e_steps = 3 if not args.small else 10

@@ -1,0 +1,74 @@
+"""The multi-process host logic of bench.py on CPU: two gloo ranks agree on
+the slowest rank's time and on the whole-job value, and under torchrun only
+rank 0 of the reference arm does any work."""
+from __future__ import annotations
+
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank: int, world: int, port: int, q) -> None:
+    import torch
+    import torch.distributed as dist
+
+    sys.path.insert(0, ROOT)
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+
+        ms = 10.0 + 5.0 * rank  # rank 1 is the slow one
+        slowest = bench._max_over_ranks(ms, torch.device("cpu"))
+        q.put((rank, slowest, bench._job_value(world, 1_000_000, 4, slowest)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_time():
+    import torch.multiprocessing as mp
+
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    out.sort()
+    assert [o[1] for o in out] == [15.0, 15.0]
+    # 2 ranks x 1e6 bytes x 4 steps over 15 ms
+    assert all(o[2] == pytest.approx(2 * 1_000_000 * 4 / 15e-3 / 1e9) for o in out)
+
+
+def test_single_process_value_is_its_own():
+    sys.path.insert(0, ROOT)
+    import torch
+
+    import bench
+
+    assert bench._max_over_ranks(3.5, torch.device("cpu")) == 3.5
+    assert bench._job_value(1, 2_000_000_000, 10, 1000.0) == pytest.approx(20.0)
+
+
+def test_reference_arm_runs_on_rank_0_only():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2"], cwd=ROOT, env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
