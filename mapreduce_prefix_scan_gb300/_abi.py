@@ -38,11 +38,14 @@ class ak_opts(ctypes.Structure):
 _lib = None
 
 
-def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libak.so and declare its prototypes."""
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libak.so (LIB_PATH unless a path is given) and declare its
+    prototypes. There is no fallback: without the library every call raises."""
     global _lib
-    if _lib is not None:
-        return _lib
+    if path is None:
+        if _lib is not None:
+            return _lib
+        path = LIB_PATH
     if not os.path.exists(path):
         raise ImportError(f"libak.so not built ({path}); run __graft_entry__.build() or "
                           "python -m mapreduce_prefix_scan_gb300.build")
@@ -73,5 +76,6 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     for f in ("ak_reduce_workspace_size", "ak_reduce", "ak_reduce_dims_workspace_size", "ak_reduce_dims",
               "ak_accumulate_workspace_size", "ak_accumulate", "ak_dims_select", "ak_reduce_noalloc"):
         getattr(L, f).restype = I32
-    _lib = L
+    if path == LIB_PATH:
+        _lib = L
     return L

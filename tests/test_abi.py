@@ -126,3 +126,16 @@ def test_dims_selector(L):
     assert ak.ak_dims_select(3072, 2048, 1, 2, 8, 152, "thread")[2] == 1
     with pytest.raises(ak.AkError):
         ak.ak_dims_select(0, 1, 1, 4, 4, 152)
+
+
+def test_missing_library_fails_loudly():
+    # no CPU or PyTorch fallback: without libak.so every entry point raises
+    import subprocess
+    import sys
+
+    code = ("import mapreduce_prefix_scan_gb300._abi as a; a.LIB_PATH = '/nonexistent/libak.so'; "
+            "import mapreduce_prefix_scan_gb300 as ak; ak.ak_reduce_workspace_size(100, \"f32\", \"f32\")")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert "libak.so not built" in r.stderr
