@@ -1,6 +1,7 @@
 // ak_common.cuh -- sm_103a building blocks shared by the reduce and scan
-// kernels: streaming vector loads, release/acquire flag access, programmatic
-// dependent launch, and ordered warp / block combines of partial results.
+// kernels: streaming and L2-policy vector loads and stores, relaxed flag
+// reads, the global timer, programmatic dependent launch, and ordered warp /
+// block combines of partial results.
 #pragma once
 
 #include <cstdint>
@@ -98,43 +99,13 @@ __device__ __forceinline__ void st_hint32(void* p, const Raw<32>& r, uint64_t po
                  : "memory");
 }
 
-// Plain 16-byte global store that does not allocate in L1.
-__device__ __forceinline__ void st_global16(void* p, const Raw<16>& r) {
-    asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(r.w[0]),
-                 "r"(r.w[1]), "r"(r.w[2]), "r"(r.w[3])
-                 : "memory");
-}
-
 // --------------------------------------------------------------------------
 // inter-block communication
 // --------------------------------------------------------------------------
 
-__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
-    uint64_t v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
 __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
     uint64_t v;
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Load of a value published by another block: read at L2 (the point of
-// coherence), never from a possibly stale L1 line.
-template <class T>
-__device__ __forceinline__ T ld_coherent(const T* p) {
-    static_assert(sizeof(T) % 4 == 0, "word-sized types only");
-    T v;
-    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
-    const uint32_t* s = reinterpret_cast<const uint32_t*>(p);
-#pragma unroll
-    for (int i = 0; i < (int)(sizeof(T) / 4); ++i) w[i] = __ldcg(s + i);
     return v;
 }
 
