@@ -109,6 +109,13 @@ __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
     return v;
 }
 
+// a / b for a >= 0 and b > 0, in 32-bit arithmetic when both fit (a 64-bit
+// division is a long emulated instruction sequence on the GPU).
+__device__ __forceinline__ int64_t div_fast(int64_t a, int64_t b) {
+    if (((uint64_t)a | (uint64_t)b) < (1ull << 32)) return (int64_t)((uint32_t)a / (uint32_t)b);
+    return a / b;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -90,16 +90,16 @@ __global__ void __launch_bounds__(kBlock) k_dims_strided(const In* __restrict__ 
     constexpr int V = VB / (int)sizeof(In);
     __shared__ P smem[kBlock * V];
 
-    const int64_t tiles_i = (I + tile_out - 1) / tile_out;
+    const int64_t tiles_i = div_fast(I + tile_out - 1, tile_out);
     const int64_t tile_id = CLUSTER ? blockIdx.x / split : blockIdx.x;
-    const int64_t ct = tile_id % tiles_i, k = tile_id / tiles_i;
+    const int64_t k = div_fast(tile_id, tiles_i), ct = tile_id - k * tiles_i;
     const int s = CLUSTER ? (int)(blockIdx.x % split) : (int)blockIdx.y;
     const int tid = threadIdx.x, c = tid % tpr, rg = tid / tpr;
     const int64_t i0 = ct * tile_out + (int64_t)c * V;
 
-    const int64_t jper = (J + split - 1) / split;
+    const int64_t jper = div_fast(J + split - 1, split);
     const int64_t js = (int64_t)s * jper, je = min(J, js + jper);
-    const int64_t rper = (je - js + R - 1) / R;
+    const int64_t rper = div_fast(max(je - js, (int64_t)0) + R - 1, R);
     const int64_t jr = min(je, js + rg * rper), jre = min(je, jr + rper);
 
     P acc[V];
@@ -191,9 +191,9 @@ __global__ void __launch_bounds__(kBlock) k_dims_rows(const In* __restrict__ x, 
     const int lane = threadIdx.x % kWarp;
     const int64_t gw = (int64_t)blockIdx.x * (kBlock / kWarp) + threadIdx.x / kWarp;
     if (gw >= K * split) return;
-    const int64_t k = gw / split;
-    const int s = (int)(gw % split);
-    const int64_t jper = (J + split - 1) / split;
+    const int64_t k = div_fast(gw, split);
+    const int s = (int)(gw - k * split);
+    const int64_t jper = div_fast(J + split - 1, split);
     const int64_t js = (int64_t)s * jper, je = min(J, js + jper);
     const In* row = x + J * k;
     P a = M::empty();

@@ -246,6 +246,21 @@ __device__ __forceinline__ int64_t claim_tile(const ScanCtl& ctl, int64_t ntiles
     return (int64_t)atomicAdd(ctl.counter, 1ull);
 }
 
+// Position of tile k in its line (t = k mod tiles_per_line, line = k div
+// tiles_per_line): no 64-bit division (a long emulated sequence on the GPU)
+// when the array is one line, one division otherwise.
+__device__ __forceinline__ void tile_pos(int64_t k, int64_t tiles_per_line, int64_t ntiles, int64_t* t,
+                                         int64_t* line) {
+    if (tiles_per_line >= ntiles) {
+        *t = k;
+        *line = 0;
+    } else {
+        const int64_t q = k / tiles_per_line;
+        *line = q;
+        *t = k - q * tiles_per_line;
+    }
+}
+
 // Ordered combine over the block (thread 0 leftmost); result in thread 0;
 // ends with the block in sync.
 template <class M, int BLOCK>
@@ -716,8 +731,9 @@ __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Ac
         P agg = M::empty();
         if (k < ntiles) {
             // ---- phase A of super-tile k
-            const int64_t t = k % tiles_per_line;
-            const int64_t start = (k / tiles_per_line) * len + t * SUPER;
+            int64_t t, line;
+            tile_pos(k, tiles_per_line, ntiles, &t, &line);
+            const int64_t start = line * len + t * SUPER;
             const int64_t cnt = min(SUPER, len - t * SUPER);
             const int n = (int)max((int64_t)0, min((int64_t)SEG, cnt - (int64_t)tid * SEG));
             const P tot = n > 0 ? segment_fold<In, M, SEG>(x + start + (int64_t)tid * SEG, n, keep) : M::empty();
@@ -734,8 +750,9 @@ __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Ac
         if (prev >= 0) {
             // ---- phase B of super-tile prev
             const int pslot = slot ^ 1;
-            const int64_t t = prev % tiles_per_line;
-            const int64_t start = (prev / tiles_per_line) * len + t * SUPER;
+            int64_t t, line;
+            tile_pos(prev, tiles_per_line, ntiles, &t, &line);
+            const int64_t start = line * len + t * SUPER;
             const int64_t cnt = min(SUPER, len - t * SUPER);
             P prefix = has_init ? M::lift(init) : M::empty();
             if (t != 0) {
@@ -957,6 +974,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     __shared__ __align__(8) uint64_t full[S], folded[S], ready[S], empty[S];
     __shared__ int64_t s_k[S];
     __shared__ int64_t s_kprev[S];  // the block's tile before s_k[s] (-1: none)
+    __shared__ int64_t s_t[S];      // position of s_k[s] in its line
+    __shared__ int64_t s_base[S];   // element offset of the tile's first row
     __shared__ P s_agg[S];
     __shared__ P s_pre[S];
     __shared__ P fwt[ROWS / 32];
@@ -969,13 +988,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
     const int64_t rem = len - rows_full * R;  // elements of the partial last row (a single line only)
 
-    auto row_count = [&](int64_t k, int r) -> int {
-        const int64_t row = (k % tiles_per_line) * ROWS + r;
+    // valid elements of row r of the tile in stage s, and the row's element
+    // offset (tile positions are worked out once, by the producer)
+    auto row_count = [&](int s, int r) -> int {
+        const int64_t row = s_t[s] * ROWS + r;
         return row < rows_full ? R : (row == rows_full ? (int)rem : 0);
     };
-    auto row_off = [&](int64_t k, int r) -> int64_t {
-        return (k / tiles_per_line) * len + ((k % tiles_per_line) * ROWS + r) * R;
-    };
+    auto row_off = [&](int s, int r) -> int64_t { return s_base[s] + (int64_t)r * R; };
 
     if (tid == 0) {
 #pragma unroll
@@ -1014,10 +1033,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 break;
             }
             next = atomicAdd(ctl.counter, 1ull);
-            const int64_t row0 = (k % tiles_per_line) * ROWS;
+            int64_t t, line;
+            tile_pos(k, tiles_per_line, ntiles, &t, &line);
+            const int64_t row0 = t * ROWS;
+            s_t[s] = t;
+            s_base[s] = line * len + row0 * R;
             if (row0 < rows_full) {
                 mbar_arrive_expect_tx(&full[s], TILE_BYTES);
-                tma_load_3d(bufs + (size_t)s * TILE_BYTES, &tin, 0, (int)row0, (int)(k / tiles_per_line), &full[s]);
+                tma_load_3d(bufs + (size_t)s * TILE_BYTES, &tin, 0, (int)row0, (int)line, &full[s]);
             } else {
                 mbar_arrive(&full[s]);  // only the partial row: nothing to copy
             }
@@ -1080,7 +1103,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 if (lane == 0) give_up(ctl);
                 return;
             }
-            const int64_t t = k % tiles_per_line, first = k - t, kp = s_kprev[s];
+            const int64_t t = s_t[s], first = k - t, kp = s_kprev[s];
             const bool chained = t != 0 && kp >= first;  // prefix continues from the block's previous tile
             const int64_t lo = t == 0 ? k : (chained ? kp + 1 : first);
             // fold the aggregates of tiles lo .. k-1 in order
@@ -1172,14 +1195,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 if (r == 0) mbar_arrive(&folded[s]);
                 return;
             }
-            const int nt = row_count(k, r);
+            const int nt = row_count(s, r);
             P tot = M::empty();
             if (nt == R) {
                 T run[R];
                 row_load(run, bufs + (size_t)s * TILE_BYTES, r);
                 tot = M::lift(row_fold<M>(run));
             } else if (nt > 0) {
-                const T* src = x + row_off(k, r);
+                const T* src = x + row_off(s, r);
                 for (int i = 0; i < nt; ++i) tot = M::combine(tot, M::lift(src[i]));
             }
             const P inc = warp_inclusive_scan<M>(tot, lane);
@@ -1187,21 +1210,20 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             if (lane == 0) lane_excl = M::empty();
             if (lane == kWarp - 1) fwt[fw] = inc;
             group_sync(1, ROWS);
-            if (fw == 0) {
-                const P wv = lane < ROWS / 32 ? fwt[lane] : M::empty();
-                const P wi = warp_inclusive_scan<M>(wv, lane);
-                P we = shfl_up_any(wi, 1);
-                if (lane == 0) we = M::empty();
-                const P agg = shfl_idx_any(wi, ROWS / 32 - 1);
-                if (lane < ROWS / 32) fwt[lane] = we;
-                if (lane == 0) {
-                    s_agg[s] = agg;
-                    const int64_t t = k % tiles_per_line;
-                    if (t != tiles_per_line - 1 && k != ctl.skip_tile) publish(ts, k, kStatusAggregate, agg, ctl.epoch);
-                }
+            // every warp folds the warp totals before its own (at most 7
+            // combines), the first thread all of them: no second hand-off
+            P base = M::empty();
+#pragma unroll
+            for (int w = 0; w < ROWS / 32; ++w)
+                if (w < fw) base = M::combine(base, fwt[w]);
+            if (r == 0) {
+                P agg = base;
+#pragma unroll
+                for (int w = 0; w < ROWS / 32; ++w) agg = M::combine(agg, fwt[w]);
+                s_agg[s] = agg;
+                if (s_t[s] != tiles_per_line - 1 && k != ctl.skip_tile) publish(ts, k, kStatusAggregate, agg, ctl.epoch);
             }
-            group_sync(1, ROWS);
-            rowpre[(size_t)s * ROWS + r] = M::combine(fwt[fw], lane_excl);
+            rowpre[(size_t)s * ROWS + r] = M::combine(base, lane_excl);
             group_sync(1, ROWS);  // every row prefix written; fwt free again
             if (r == 0) mbar_arrive(&folded[s]);
         }
@@ -1221,15 +1243,15 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             const int64_t k = s_k[s];
             if (k >= ntiles) return;
             const P from = M::combine(s_pre[s], rowpre[(size_t)s * ROWS + r]);
-            const int nt = row_count(k, r);
+            const int nt = row_count(s, r);
             if (nt == R) {
                 T run[R];
                 row_load(run, bufs + (size_t)s * TILE_BYTES, r);
                 row_scan_from<M>(run, from);
-                row_store_global(y + row_off(k, r), run, last_use);
+                row_store_global(y + row_off(s, r), run, last_use);
             } else if (nt > 0) {
-                const T* src = x + row_off(k, r);
-                T* dst = y + row_off(k, r);
+                const T* src = x + row_off(s, r);
+                T* dst = y + row_off(s, r);
                 P a = from;
                 for (int i = 0; i < nt; ++i) {
                     a = M::combine(a, M::lift(src[i]));
