@@ -40,6 +40,17 @@ def test_cumsum_1e8_f64():
     assert_close_f32(y, want, np.cumsum(x), rel=F64_REL)
 
 
+def test_cumsum_1e8_f32_and_i64():
+    # the bench's f32 scan (the TMA pipeline) at full size, and the integer
+    # scan through the same pipeline, bit-exact
+    x = synth.normal_f32(10**8, seed=0, stream=65)
+    y = ak.ak_accumulate(dev_of("f32", x)).cpu().numpy()
+    assert_close_f32(y, oracle.scan(x, "f32"), np.cumsum(np.abs(x.astype(np.float64))))
+    del x, y
+    xi = synth.uniform_int(5 * 10**7, -(2**20), 2**20, np.int64, seed=0, stream=3)
+    assert_exact(ak.ak_accumulate(dev_of("i64", xi)).cpu().numpy(), oracle.scan(xi, "i64"))
+
+
 def test_accumulate_max_1e7_f32_no_neutral():
     x = synth.normal_f32(10**7, seed=0, stream=61)
     y = ak.ak_accumulate(dev_of("f32", x), op="max", opts=ak.make_opts(no_neutral=True)).cpu().numpy()
