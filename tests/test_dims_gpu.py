@@ -183,3 +183,20 @@ def test_empty_reductions():
         ak.ak_reduce_dims(x, [1], op="max")
     out = ak.ak_reduce_dims(torch.empty((3, 0), device="cuda"), [1])  # no outputs
     assert out.numel() == 0
+
+
+def test_mat2_dims_results_are_canonical():
+    p = synth.MODP
+    shape = (40, 600, 3)
+    n = int(np.prod(shape))
+    x = np.zeros((n, 4), dtype=np.int32)
+    x[:, 0] = 1
+    x[:, 3] = 1
+    # along the reduced (middle) dimension the a12 entries alternate p-1, 1
+    j = (np.arange(n) // shape[0]) % shape[1]
+    x[:, 2] = np.where(j % 2 == 0, p - 1, 1)
+    for forced in ("auto", "thread", "columns"):
+        got = _run(x, "mat2", shape, [1], op="matmul", opts=ak.make_opts(dims_shape=forced))
+        g = got.cpu().numpy().view(np.uint32).reshape(-1, 4)
+        assert g.max() < p
+        assert_exact(g, oracle.reduce_dims(x, "mat2", shape, [1]))

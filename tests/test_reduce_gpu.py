@@ -246,3 +246,21 @@ def test_workspace_reuse_and_target_blocks():
         opts = ak.make_opts(target_blocks=tb)
         got = ak.ak_reduce(xd, to_host=True, workspace=ws, opts=opts)
         assert abs(got - want) <= 2.0**-45 * _absmass(x, "f64", "identity")
+
+
+def test_mat2_reduction_results_are_canonical():
+    # a product whose lazily reduced entries land on p (see the scan test of
+    # the same name): the stored result is reduced below p, device and host
+    p = synth.MODP
+    for n in (10_000, 1_000_001):
+        x = np.zeros((n, 4), dtype=np.int32)
+        x[:, 0] = 1
+        x[:, 3] = 1
+        x[0::2, 2] = p - 1
+        x[1::2, 2] = 1
+        xd = dev_of("mat2", x)
+        want = tuple(int(v) for v in oracle.reduce(x, "mat2"))
+        d = torch.empty(4, dtype=torch.int32, device="cuda")
+        ak.ak_reduce(xd, op="matmul", elem="mat2", dst=d)
+        assert tuple(int(v) for v in d.cpu().numpy().view(np.uint32)) == want
+        assert ak.ak_reduce(xd, op="matmul", elem="mat2", to_host=True) == want

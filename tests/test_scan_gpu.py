@@ -298,3 +298,26 @@ def test_lookback_wait_runs_out_and_gpu_stays_usable():
     assert ei.value.status == 6
     y = ak.ak_accumulate(xd, opts=ak.make_opts(check=True)).cpu().numpy()
     assert_close_f32(y, oracle.scan(x, "f64"), np.cumsum(np.abs(x)), rel=F64_REL)
+
+
+def _mat2_hitting_p(n):
+    # alternating [[1, p-1], [0, 1]] and [[1, 1], [0, 1]] (column-major
+    # a11, a21, a12, a22): every second prefix has a12 = p - 1 + 1 = 0 mod p,
+    # which an uncanonicalised product leaves as p
+    p = synth.MODP
+    x = np.zeros((n, 4), dtype=np.int32)
+    x[:, 0] = 1
+    x[:, 3] = 1
+    x[0::2, 2] = p - 1
+    x[1::2, 2] = 1
+    return x
+
+
+@pytest.mark.parametrize("shape,dim", [((50_001,), -1), ((1000, 40), 0), ((3, 20_000), 1), ((20_000, 3), 0)])
+def test_mat2_results_are_canonical(shape, dim):
+    n = int(np.prod(shape))
+    x = _mat2_hitting_p(n)
+    xd = dev_of("mat2", x).reshape(tuple(reversed(shape)) + (4,))
+    y = ak.ak_accumulate(xd, dim=dim, op="matmul", elem="mat2").cpu().numpy().view(np.uint32).reshape(-1, 4)
+    assert y.max() < synth.MODP
+    assert_exact(y, oracle.scan(x, "mat2", shape, dim))
