@@ -300,6 +300,21 @@ def test_lookback_wait_runs_out_and_gpu_stays_usable():
     assert_close_f32(y, oracle.scan(x, "f64"), np.cumsum(np.abs(x)), rel=F64_REL)
 
 
+def test_lookback_wait_runs_out_on_the_tma_path():
+    # The same injected missing publication on the TMA pipeline (i64, 4096
+    # elements per tile): the look-back warp that needs tile 5's aggregate
+    # gives up after 20 ms, every other role sees the error word and leaves,
+    # the producer lets its copies land; the next call is correct.
+    x = gen("i64", 40 * 4096 + 17, stream=77)
+    xd = dev_of("i64", x)
+    opts = ak.make_opts(check=True, wait_limit_ns=20_000_000, debug_skip_publish_tile=5)
+    with pytest.raises(ak.AkError) as ei:
+        ak.ak_accumulate(xd, opts=opts)
+    assert ei.value.status == 6
+    y = ak.ak_accumulate(xd, opts=ak.make_opts(check=True)).cpu().numpy()
+    assert_exact(y, oracle.scan(x, "i64"))
+
+
 def _mat2_hitting_p(n):
     # alternating [[1, p-1], [0, 1]] and [[1, 1], [0, 1]] (column-major
     # a11, a21, a12, a22): every second prefix has a12 = p - 1 + 1 = 0 mod p,
