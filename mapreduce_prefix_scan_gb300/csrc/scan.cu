@@ -1,35 +1,42 @@
 // scan.cu -- inclusive scans (accumulate!, cumsum) on GB300.
 //
-// Contiguous lines (the whole array, or every line along dimension 0) take a
-// single-pass tile scan; lines along a strided dimension take a
-// column-parallel kernel.
+// Four kernels, chosen per call:
+//
+//  * k_scan_tma -- long contiguous lines of f32 / i32 / i64 with a neutral
+//    element: one persistent block per SM runs a ring of 32 KB tiles copied
+//    by the TMA engine through producer, fold, look-back and scan warps
+//    (described at the kernel). Every element is read once and written once.
+//  * k_scan_tiles -- other long contiguous lines (f64, the matrix product,
+//    Optional partials, mixed input and accumulator types): persistent
+//    blocks claim super-tiles, fold them (phase A) and scan them one round
+//    later from L2 (phase B).
+//  * k_scan_lines -- lines that fit one tile (e.g. dims=1 of a matrix):
+//    one block per line, no state shared between blocks.
+//  * k_scan_strided -- lines along a strided dimension: a thread per column.
 //
 // Tile scan (AcceleratedKernels.jl tile-scan PR #202, first two
-// paragraphs): a tile is loaded striped (coalesced), each thread scans its
-// own run of `items` consecutive elements, the run totals are scanned across
-// the block, and the tile's prefix is applied. Runs sit in shared memory at
-// an odd stride so that the threads of a warp reading their runs spread over
-// the banks. GB300 version of that padding: the stride is odd in 16-byte
-// units (one 16-byte pad after a run whose length is an even number of
-// 16-byte chunks), which keeps every run 16-byte aligned, so runs of any
-// element size are read and written with 128-bit shared accesses and 8
-// consecutive threads hit 8 distinct bank quads.
+// paragraphs): a tile is loaded, each thread scans its own run of
+// consecutive elements, the run totals are scanned across the block, and
+// the tile's prefix is applied. For lines that fit one tile the runs sit in
+// shared memory at an odd stride, as there; the GB300 version of that
+// padding is one 16-byte pad after a run whose length is an even number of
+// 16-byte chunks, which keeps every run 16-byte aligned, so runs of any
+// element size move with 128-bit shared accesses and 8 consecutive threads
+// hit 8 distinct bank quads. The TMA path gets the same effect from the
+// copy engine's 128-byte swizzle.
 //
-// Tiles pass prefixes on in one pass with decoupled look-back (Merrill &
-// Garland, "Single-pass Parallel Prefix Scan with Decoupled Look-back",
-// 2016): a tile publishes its aggregate, a warp inspects up to 32
-// predecessors at a time, folds aggregates back to the nearest published
-// inclusive prefix, then publishes its own inclusive prefix. One block per
-// tile, several blocks per SM, so one tile's look-back hides behind other
-// tiles' loads. A block takes its tile index from an atomic counter when it
-// starts, so every tile it waits for belongs to a block that is already
-// running: progress never depends on the order in which the hardware
-// dispatches blocks. Each call clears the counter and the tile records on its
-// own stream before the kernel (so a call captured in a CUDA graph is correct
-// on every replay), and every record also carries the call's epoch. Every
-// wait is bounded by a global-timer deadline; a block that gives up records
-// the epoch in the workspace's error word, which every other waiter also
-// watches, and all blocks leave early.
+// Tile prefixes cross tiles in one pass from published tile records (after
+// Merrill & Garland, "Single-pass Parallel Prefix Scan with Decoupled
+// Look-back", 2016). Tile indices come from an atomic counter claimed by
+// running blocks, so every tile a block waits for belongs to a block that
+// is already running: progress never depends on the order in which the
+// hardware dispatches blocks. Each call clears the counter and the tile
+// records on its own stream before the kernel (so a call captured in a CUDA
+// graph is correct on every replay), and every record also carries the
+// call's epoch and a check word. Every wait is bounded by a global-timer
+// deadline; a block that gives up records the epoch in the workspace's
+// error word, which every other waiter also watches, and all blocks leave
+// early.
 #include <algorithm>
 #include <atomic>
 #include <mutex>
