@@ -131,8 +131,10 @@ typedef struct ak_opts {
 /* AK_FLAG_DIMS_CLUSTER: a strided dims reduction whose split fits 2..16
  * blocks runs each output tile's blocks as one thread-block cluster and
  * combines their partials in distributed shared memory (one kernel, no
- * workspace partials) instead of a workspace and a second pass. Off by
- * default: on GB300 the second pass measured faster at every tested shape. */
+ * workspace partials) instead of a workspace and a second pass, at any input
+ * size. Without the flag the automatic shape does so only for inputs of at
+ * most 16 MB, where saving the second launch pays on GB300; larger inputs
+ * split through the workspace. */
 #define AK_FLAG_DIMS_CLUSTER 1
 
 void ak_opts_default(ak_opts* opts);

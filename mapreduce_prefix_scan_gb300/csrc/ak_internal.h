@@ -170,7 +170,8 @@ struct DimsCall {
     void* ws;
     size_t ws_bytes;
     int forced_shape;
-    bool allow_cluster;
+    bool allow_cluster;  // AK_FLAG_DIMS_CLUSTER: combine split blocks in a cluster whenever one fits
+    bool auto_cluster;   // auto shape: combine in a cluster for small inputs (see select_shape)
     cudaStream_t stream;
     // general fallback (any dims mask): full shape and mask
     int ndim;

@@ -406,6 +406,7 @@ ak_status setup_dims(const void* src, int ndim, const int64_t* shape, uint32_t m
     d->c.no_neutral = o.no_neutral != 0;
     d->c.forced_shape = o.dims_shape;
     d->c.allow_cluster = (o.flags & AK_FLAG_DIMS_CLUSTER) != 0;
+    d->c.auto_cluster = true;
     d->c.ndim = ndim;
     d->c.mask = mask;
     for (int i = 0; i < ndim; ++i) d->c.shape[i] = shape[i];
@@ -431,11 +432,33 @@ extern "C" ak_status ak_reduce_dims_workspace_size(int ndim, const int64_t* shap
     if (!bytes || !valid_dtype(in) || !valid_dtype(acc)) return AK_ERR_INVALID_ARG;
     if (opts && (opts->dims_shape < AK_SHAPE_AUTO || opts->dims_shape > AK_SHAPE_COLUMNS)) return AK_ERR_INVALID_ARG;
     const ak_opts o = resolve_opts(opts);
-    DimsSetup d;
-    // the vector width depends on the source alignment; assume aligned
-    ak_status s = setup_dims(reinterpret_cast<const void*>(uintptr_t(256)), ndim, shape, dims_mask, in, acc, o, &d);
-    if (s != AK_OK) return s;
-    *bytes = d.ws_bytes;
+    // The plan depends on the source alignment (vector width) and on whether
+    // a cluster fits; report the largest workspace any of them needs: an
+    // aligned and an element-aligned source, with and without the cluster
+    // combine.
+    size_t most = 0;
+    for (int variant = 0; variant < 4; ++variant) {
+        ak_opts ov = o;
+        if (variant & 2) ov.flags &= ~AK_FLAG_DIMS_CLUSTER;
+        DimsSetup d;
+        const uintptr_t addr = 256 + ((variant & 1) ? ak_dtype_size(in) : 0);
+        ak_status s = setup_dims(reinterpret_cast<const void*>(addr), ndim, shape, dims_mask, in, acc, ov, &d);
+        if (s != AK_OK) return s;
+        if (variant & 2) {
+            // the same call planned without the cluster combine
+            d.c.auto_cluster = false;
+            d.c.allow_cluster = false;
+            if (d.path != 1 && d.cn.nout != 0 && d.cn.nfold != 0) {
+                DeviceInfo dev;
+                if (!current_device(&dev)) return AK_ERR_CUDA;
+                s = plan_dims(d.c, dev, &d.dplan);
+                if (s != AK_OK) return s;
+                d.ws_bytes = d.dplan.ws_bytes;
+            }
+        }
+        most = std::max(most, d.ws_bytes);
+    }
+    *bytes = most;
     return AK_OK;
 }
 

@@ -20,6 +20,7 @@ namespace {
 using dims::kBlock;
 using dims::kMinRowsPerGroup;
 constexpr int kMaxCluster = 16;
+constexpr int64_t kClusterAutoBytes = (int64_t)16 << 20;  // default cluster combine up to this input size
 // fewest reduction rows a block of a cluster should get
 constexpr int64_t R_rows_min(int row_groups) { return (int64_t)row_groups * 2; }
 
@@ -37,7 +38,7 @@ __global__ void k_fill(Out* dst, int64_t count, Out v) {
 // to give the device about target_ctas blocks, and never below
 // kMinRowsPerGroup rows per group.
 static void select_shape(int64_t I, int64_t J, int64_t K, int esz, int vec, int sm_count, int forced,
-                         bool allow_cluster, DimsPlan* p) {
+                         bool allow_cluster, bool auto_cluster, DimsPlan* p) {
     const int64_t vecs_per_row = (I + vec - 1) / vec;
     // Enough outputs that one thread per vector of outputs already puts
     // kUnroll loads in flight on every thread slot of the device.
@@ -65,7 +66,14 @@ static void select_shape(int64_t I, int64_t J, int64_t K, int esz, int vec, int 
         p->row_groups = kBlock / tpr;
         return ((I + p->tile_out - 1) / p->tile_out) * K;  // output tiles
     };
-    if (shape == AK_SHAPE_COLUMNS && allow_cluster) {
+    // The split blocks of an output tile combine in a thread-block cluster
+    // (no workspace, no second launch) on request, and by default for
+    // inputs of at most kClusterAutoBytes: there the second launch is a
+    // large part of the call (3072 x 2048 bf16 back to back: 7.2 against
+    // 7.8 us), while on larger inputs the smaller clusters' longer row
+    // ranges cost more than the launch they save.
+    const bool cluster_ok = allow_cluster || (auto_cluster && forced == AK_SHAPE_AUTO && bytes <= kClusterAutoBytes);
+    if (shape == AK_SHAPE_COLUMNS && cluster_ok) {
         // Prefer a cluster split (2..16 blocks per output tile, partials
         // combined in distributed shared memory): try row segments of 32,
         // 16, 8 and 4 threads until the wanted split fits a cluster.
@@ -125,7 +133,8 @@ ak_status plan_dims(const DimsCall& c, const DeviceInfo& dev, DimsPlan* p) {
         const uintptr_t addr = reinterpret_cast<uintptr_t>(c.src);
         int vec = 1;
         if (esz < 16 && addr % 16 == 0 && (c.inner * (int64_t)esz) % 16 == 0) vec = (int)(16 / esz);
-        select_shape(c.inner, c.red, c.outer, (int)esz, vec, dev.sm_count, c.forced_shape, c.allow_cluster, p);
+        select_shape(c.inner, c.red, c.outer, (int)esz, vec, dev.sm_count, c.forced_shape, c.allow_cluster,
+                     c.auto_cluster, p);
     }
     if (p->split > 1 && !p->cluster)
         p->ws_bytes = align_up(kWsHeader + (size_t)p->split * c.inner * c.outer * psz, 256);
@@ -168,7 +177,7 @@ extern "C" ak_status ak_dims_select(int64_t inner, int64_t red_len, int64_t oute
         forced_shape < AK_SHAPE_AUTO || forced_shape > AK_SHAPE_COLUMNS || vec_elems * elem_bytes > 16)
         return AK_ERR_INVALID_ARG;
     ak::DimsPlan p = {};
-    ak::select_shape(inner, red_len, outer, elem_bytes, vec_elems, sm_count, forced_shape, false, &p);
+    ak::select_shape(inner, red_len, outer, elem_bytes, vec_elems, sm_count, forced_shape, false, true, &p);
     if (shape_out) *shape_out = p.shape;
     if (tile_outputs) *tile_outputs = p.tile_out;
     if (row_groups) *row_groups = p.row_groups;

@@ -110,10 +110,15 @@ def test_accumulate_validates_and_plans_on_host(L):
 
 def test_dims_selector(L):
     import mapreduce_prefix_scan_gb300 as ak
-    # 3072 x 2048 bf16, dims=2: 16-byte vectors of 8, a warp across a
-    # 256-output row segment, 8 row groups, the reduction split so that the
-    # device gets >= 1 block per SM
+    # 3072 x 2048 bf16, dims=2 (12.6 MB): 16-byte vectors of 8, 16 threads
+    # across a 128-output row segment, 16 row groups, the reduction split 16
+    # ways and the split blocks of an output tile combined in a thread-block
+    # cluster (small inputs)
     shape, tile, groups, split = ak.ak_dims_select(3072, 2048, 1, 2, 8, 152)
+    assert shape == "columns" and tile == 128 and groups == 16 and split == 16
+    # a larger input: a warp across a 256-output row segment, 8 row groups,
+    # split through the workspace and a second pass, >= 1 block per SM
+    shape, tile, groups, split = ak.ak_dims_select(3072, 8192, 1, 2, 8, 152)
     assert shape == "columns" and tile == 256 and groups == 8 and split > 1
     assert -(-3072 // tile) * split >= 152
     # middle dim of 64 x 4096 x 32 f32: 16 threads cover the 64 outputs of a run
