@@ -433,3 +433,92 @@ def test_signed_zero_follows_the_left_fold():
     # with an init of -0.0 the fold of -0.0 stays -0.0; a +0.0 init makes it +0.0
     assert np.signbit(oracle.reduce(np.full(3, -0.0), "f64", init=-0.0))
     assert not np.signbit(oracle.reduce(np.full(3, -0.0), "f64", init=0.0))
+
+
+# --------------------------------------------------------------------------
+# init in dims reductions and in float scans; float scans along a dimension
+# (init applied exactly once, at the left of each output's fold: "Finish
+# whole-array reductions on the device", section "Compatibility")
+# --------------------------------------------------------------------------
+
+def _colmajor_axes(shape, dims):
+    return tuple(len(shape) - 1 - d for d in dims)
+
+
+@pytest.mark.parametrize("shape,dims", [((5, 7), (1,)), ((5, 7), (0,)), ((4, 6, 3), (1,)),
+                                        ((4, 6, 3), (0, 2)), ((3, 1, 5, 2), (1, 3))])
+def test_reduce_dims_int_init_once_per_output(shape, dims):
+    n = int(np.prod(shape))
+    x = synth.uniform_int(n, -1000, 1000, np.int64, stream=50)
+    arr = x.reshape(tuple(reversed(shape)))
+    axes = _colmajor_axes(shape, dims)
+    init = 123_457
+    got = oracle.reduce_dims(x, "i64", shape, dims, init=init)
+    assert np.array_equal(got, arr.sum(axis=axes, keepdims=True).ravel() + init)
+    # max: an init above every element wins everywhere, one below none
+    assert np.all(oracle.reduce_dims(x, "i64", shape, dims, op="max", init=5000) == 5000)
+    assert np.array_equal(oracle.reduce_dims(x, "i64", shape, dims, op="max", init=-5000),
+                          arr.max(axis=axes, keepdims=True).ravel())
+    # product: init * prod(x) per output, wrapped to 64 bits (exact Python ints)
+    xs = synth.uniform_int(n, -3, 3, np.int64, stream=51)
+    got = oracle.reduce_dims(xs, "i64", shape, dims, op="mul", init=7)
+    prods = np.ravel(np.prod(xs.reshape(tuple(reversed(shape))).astype(object), axis=axes, keepdims=True))
+    assert [int(v) for v in got] == [((7 * int(p) + 2**63) % 2**64) - 2**63 for p in prods]
+
+
+def test_reduce_dims_float_init_once_per_output():
+    shape = (6, 50, 4)
+    x = synth.uniform_f32_pm1(int(np.prod(shape)), stream=52)
+    arr = x.astype(np.float64).reshape(4, 50, 6)
+    for init in (0.375, -1.5):
+        got = oracle.reduce_dims(x, "f32", shape, (1,), init=init)
+        for k in range(4):
+            for i in range(6):
+                assert got[i + 6 * k] == math.fsum([init] + list(arr[k, :, i]))
+    # abs2 applies to the elements, not to init
+    got = oracle.reduce_dims(x, "f32", shape, (1,), map="abs2", init=-2.0)
+    assert got[0] == math.fsum([-2.0] + list(arr[0, :, 0] ** 2))
+    # empty reduced extent: every output is init
+    assert np.all(oracle.reduce_dims(np.zeros(0, np.float32), "f32", (3, 0), (1,), init=2.5) == 2.5)
+
+
+def test_reduce_dims_mat2_init_on_the_left():
+    shape = (3, 5)
+    x = synth.mat2_modp(15, stream=53)
+    init = synth.mat2_modp(1, stream=54)[0]
+    r = oracle.reduce_dims(x, "mat2", shape, (1,), init=init)
+    for i in range(3):
+        assert list(r[i]) == _exact_product([init] + list(x[i::3]))
+    r = oracle.reduce_dims(x, "mat2", shape, (0,), init=init)
+    for j in range(5):
+        assert list(r[j]) == _exact_product([init] + list(x[3 * j: 3 * j + 3]))
+
+
+@pytest.mark.parametrize("shape,dim", [((5, 7), 0), ((5, 7), 1), ((3, 4, 5), 1), ((3, 4, 5), 2)])
+def test_float_scan_along_dim_matches_fsum_prefixes(shape, dim):
+    n = int(np.prod(shape))
+    x = synth.uniform_f32_pm1(n, stream=55)  # 2^-23 grid: every prefix is exact in f64
+    arr = x.astype(np.float64).reshape(tuple(reversed(shape)))
+    ax = len(shape) - 1 - dim
+    for init in (None, 0.75):
+        y = oracle.scan(x, "f32", shape, dim, init=init).reshape(arr.shape)
+        moved = np.moveaxis(arr, ax, -1)
+        ym = np.moveaxis(y, ax, -1)
+        for idx in np.ndindex(moved.shape[:-1]):
+            line = list(moved[idx])
+            head = [] if init is None else [init]
+            for j in range(len(line)):
+                assert ym[idx][j] == math.fsum(head + line[: j + 1]), (idx, j)
+
+
+def test_float_scan_init_once_at_the_left():
+    x = synth.uniform_f32_pm1(2000, stream=56)
+    xd = x.astype(np.float64)
+    y = oracle.scan(x, "f32", init=-3.25)
+    assert np.array_equal(y, np.cumsum(np.concatenate([[-3.25], xd]))[1:])
+    # max with init: the running max never falls below init
+    ym = oracle.scan(x, "f32", op="max", init=0.5)
+    assert np.array_equal(ym, np.maximum.accumulate(np.maximum(xd, 0.5)))
+    # f64 product with init: exact powers of two
+    p = np.full(20, 2.0)
+    assert list(oracle.scan(p, "f64", op="mul", init=3.0)) == [3.0 * 2.0**k for k in range(1, 21)]
