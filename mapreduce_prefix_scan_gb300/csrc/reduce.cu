@@ -1,243 +1,18 @@
-// reduce.cu -- whole-array mapreduce on GB300.
-//
-// Design (AcceleratedKernels.jl PR #139, "Finish whole-array reductions on
-// the device", section "What changes"): at most two launches. A first pass
-// of a bounded grid in which every block reduces one contiguous share of the
-// input to one partial result, and a one-block second pass that reduces the
-// partials and performs the store (apply init, fold into R's previous value,
-// overwrite, or leave the bare partial for a host-side finish). An input
-// small enough for one block takes one launch.
-//
-// GB300 specifics: the first pass streams 32-byte vector loads
-// (ld.global.nc.v8, no L1 allocation, 256-byte L2 prefetch) with several
-// independent loads in flight per thread; the grid is a multiple of the SM
-// count; the second pass is launched with programmatic dependent launch, so
-// its launch overlaps the first pass's tail and it waits on the device
-// (griddepcontrol.wait) instead of behind a full kernel boundary.
+// reduce.cu -- host side of the whole-array mapreduce: the plan (grid and
+// workspace) and the dispatch of a call's types, operator, map and monoid to
+// the kernels of reduce.cuh.
 #include <algorithm>
 
-#include "ak_common.cuh"
-#include "ak_internal.h"
+#include "reduce.cuh"
 
 namespace ak {
-
-namespace {
-
-constexpr int kBlock = 512;       // first pass, commutative operators
-constexpr int kBlockOrd = 256;    // first pass, order-preserving
-constexpr int kFinishBlock = 256;
-constexpr int kVecBytes = 32;     // one 256-bit load per vector
-constexpr int kUnroll = 4;        // independent vector loads in flight per thread
-constexpr int kRunOrd = 8;        // consecutive elements folded per lane (ordered path)
-constexpr int kMaxBlocksPerSm = 4;
-constexpr int64_t kSingleLaunchMax = 16384;  // elements reduced by one block in one launch
-
-// Where and how the final value goes.
-template <class Acc, class Out, class M>
-struct StoreSpec {
-    int mode;          // ak_store
-    Acc init;          // for AK_STORE_INIT
-    Out* dst;          // final element (device), or null
-    typename M::P* bare;  // bare partial for the host finish, or null
-};
-
-template <class Acc, class Out, class M>
-__device__ __forceinline__ void store_result(const typename M::P& r, const StoreSpec<Acc, Out, M>& st) {
-    using Op = typename M::op;
-    if (st.bare) {
-        *st.bare = r;
-        return;
-    }
-    Acc v = M::value(r);
-    if (st.mode == AK_STORE_INIT) v = Op::apply(st.init, v);
-    else if (st.mode == AK_STORE_FOLD) v = Op::apply(convert<Acc>(*st.dst), v);
-    *st.dst = convert<Out>(v);
-}
-
-template <class In, class Acc, class Map, class M>
-__device__ __forceinline__ typename M::P lift_elem(In x) {
-    return M::lift(Map::apply(convert<Acc>(x)));
-}
-
-// First pass for commutative operators. Block b reduces the vectors
-// [b*per, (b+1)*per) of the 32-byte-aligned body; block 0 adds the unaligned
-// head and the last block the ragged tail. Thread t keeps one accumulator
-// per vector lane and folds vectors t, t+BLOCK, ... with kUnroll loads in
-// flight.
-template <class In, class Acc, class Out, class Map, class M>
-__global__ void __launch_bounds__(kBlock) k_reduce_pass1(const In* __restrict__ x, int64_t n,
-                                                         int64_t head, int64_t nvec,
-                                                         typename M::P* __restrict__ partials,
-                                                         StoreSpec<Acc, Out, M> st) {
-    using P = typename M::P;
-    constexpr int V = kVecBytes / sizeof(In);
-    __shared__ P smem[kBlock / kWarp];
-
-    P acc[V];
-#pragma unroll
-    for (int k = 0; k < V; ++k) acc[k] = M::empty();
-
-    const In* body = x + head;
-    const int64_t per = (nvec + gridDim.x - 1) / gridDim.x;
-    const int64_t vb = (int64_t)blockIdx.x * per;
-    const int64_t ve = min(nvec, vb + per);
-    int64_t v = vb + threadIdx.x;
-    for (; v + (kUnroll - 1) * kBlock < ve; v += kUnroll * kBlock) {
-        Raw<kVecBytes> r[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) r[u] = ld_stream<kVecBytes>(body + (v + u * kBlock) * V);
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-#pragma unroll
-            for (int k = 0; k < V; ++k)
-                acc[k] = M::combine(acc[k], lift_elem<In, Acc, Map, M>(raw_get<In>(r[u], k)));
-    }
-    for (; v < ve; v += kBlock) {
-        Raw<kVecBytes> r = ld_stream<kVecBytes>(body + v * V);
-#pragma unroll
-        for (int k = 0; k < V; ++k)
-            acc[k] = M::combine(acc[k], lift_elem<In, Acc, Map, M>(raw_get<In>(r, k)));
-    }
-    if (blockIdx.x == 0 && threadIdx.x < head)
-        acc[0] = M::combine(acc[0], lift_elem<In, Acc, Map, M>(x[threadIdx.x]));
-    const int64_t tail = head + nvec * V;
-    if (blockIdx.x == gridDim.x - 1 && tail + threadIdx.x < n)
-        acc[V - 1] = M::combine(acc[V - 1], lift_elem<In, Acc, Map, M>(x[tail + threadIdx.x]));
-
-    griddep_launch_dependents();
-    P a = acc[0];
-#pragma unroll
-    for (int k = 1; k < V; ++k) a = M::combine(a, acc[k]);
-    a = block_reduce<M, kBlock>(a, smem);
-    if (threadIdx.x == 0) {
-        if (gridDim.x == 1) store_result<Acc, Out, M>(a, st);
-        else partials[blockIdx.x] = a;
-    }
-}
-
-// First pass that keeps the element order (non-commutative operators). Block
-// b owns the contiguous range [b*per, (b+1)*per); each warp owns a
-// contiguous sub-range of it and walks it in chunks of 32*kRunOrd elements:
-// lane l folds its run of kRunOrd consecutive elements, the warp combines
-// the 32 runs in lane order and appends the chunk to its running value.
-// Warps are then combined in warp order.
-template <class In, class Acc, class Out, class Map, class M>
-__global__ void __launch_bounds__(kBlockOrd) k_reduce_pass1_ordered(const In* __restrict__ x,
-                                                                    int64_t n,
-                                                                    typename M::P* __restrict__ partials,
-                                                                    StoreSpec<Acc, Out, M> st) {
-    using P = typename M::P;
-    constexpr int W = kBlockOrd / kWarp;
-    __shared__ P smem[W];
-    const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
-
-    const int64_t per = (n + gridDim.x - 1) / gridDim.x;
-    const int64_t bb = (int64_t)blockIdx.x * per, be = min(n, bb + per);
-    const int64_t wper = (be - bb + W - 1) / W;
-    const int64_t wb = min(be, bb + warp * wper), we = min(be, wb + wper);
-
-    P run_acc = M::empty();  // meaningful in lane 0
-    for (int64_t c = wb; c < we; c += kWarp * kRunOrd) {
-        P r = M::empty();
-        const int64_t s = c + (int64_t)lane * kRunOrd;
-#pragma unroll
-        for (int k = 0; k < kRunOrd; ++k)
-            if (s + k < we) r = M::combine(r, lift_elem<In, Acc, Map, M>(x[s + k]));
-        r = warp_reduce<M>(r);
-        run_acc = M::combine(run_acc, r);
-    }
-    griddep_launch_dependents();
-    if (lane == 0) smem[warp] = run_acc;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        P a = smem[0];
-        for (int w = 1; w < W; ++w) a = M::combine(a, smem[w]);
-        if (gridDim.x == 1) store_result<Acc, Out, M>(a, st);
-        else partials[blockIdx.x] = a;
-    }
-}
-
-// Second pass: one block folds the partials in block order and stores.
-template <class Acc, class Out, class M>
-__global__ void __launch_bounds__(kFinishBlock) k_reduce_finish(const typename M::P* partials, int g,
-                                                                StoreSpec<Acc, Out, M> st) {
-    using P = typename M::P;
-    __shared__ P smem[kFinishBlock / kWarp];
-    griddep_wait();
-    const int per = (g + kFinishBlock - 1) / kFinishBlock;
-    const int b = threadIdx.x * per, e = min(g, b + per);
-    P a = M::empty();
-    for (int i = b; i < e; ++i) a = M::combine(a, partials[i]);
-    a = block_reduce<M, kFinishBlock>(a, smem);
-    if (threadIdx.x == 0) store_result<Acc, Out, M>(a, st);
-}
-
-template <class K, class... Args>
-cudaError_t launch_pdl(K kernel, int grid, int block, cudaStream_t s, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
-template <class In, class Acc, class Out, class Map, class M>
-ak_status launch(const ReduceCall& c, const ReducePlan& plan) {
-    using P = typename M::P;
-    StoreSpec<Acc, Out, M> st;
-    st.mode = c.mode;
-    memcpy(&st.init, c.init.b, sizeof(Acc));
-    st.dst = static_cast<Out*>(c.dst);
-    st.bare = static_cast<P*>(c.bare);
-    P* partials = reinterpret_cast<P*>(static_cast<char*>(c.ws) + plan.partials_off);
-    const In* x = static_cast<const In*>(c.src);
-    const int g = plan.grid;
-    if constexpr (M::commutative) {
-        constexpr int V = kVecBytes / sizeof(In);
-        const uintptr_t addr = reinterpret_cast<uintptr_t>(x);
-        int64_t head = (int64_t)(((kVecBytes - addr % kVecBytes) % kVecBytes) / sizeof(In));
-        head = std::min<int64_t>(head, c.n);
-        const int64_t nvec = (c.n - head) / V;
-        k_reduce_pass1<In, Acc, Out, Map, M><<<g, kBlock, 0, c.stream>>>(x, c.n, head, nvec, partials, st);
-    } else {
-        k_reduce_pass1_ordered<In, Acc, Out, Map, M><<<g, kBlockOrd, 0, c.stream>>>(x, c.n, partials, st);
-    }
-    ak_status s = check_launch();
-    if (s != AK_OK) return s;
-    count_launches(1);
-    if (g > 1) {
-        cudaError_t e = launch_pdl(k_reduce_finish<Acc, Out, M>, 1, kFinishBlock, c.stream,
-                                   (const P*)partials, g, st);
-        if (e != cudaSuccess) return cuda_fail(e);
-        count_launches(1);
-    }
-    return AK_OK;
-}
-
-}  // namespace
 
 ak_status plan_reduce(int64_t n, ak_dtype in, ak_dtype acc, bool no_neutral, int target_blocks,
                       const DeviceInfo& dev, ReducePlan* plan) {
     const size_t psz = partial_size(acc, no_neutral);
     const size_t esz = ak_dtype_size(in);
     if (psz == 0 || esz == 0) return AK_ERR_UNSUPPORTED;
-    const bool ordered = (in == AK_MAT2_MODP);
-    const int max_grid = dev.sm_count * kMaxBlocksPerSm;
-    int64_t per_block = ordered ? (int64_t)kBlockOrd * kRunOrd : (int64_t)kBlock * (kVecBytes / (int64_t)esz);
-    int64_t g = (n + per_block - 1) / per_block;
-    g = std::max<int64_t>(1, std::min<int64_t>(g, max_grid));
-    if (target_blocks > 0) g = std::min<int64_t>(g, target_blocks);
-    if (n <= kSingleLaunchMax) g = 1;
-    plan->grid = (int)g;
-    plan->partials_off = kWsHeader;
-    plan->bare_off = align_up(kWsHeader + (size_t)max_grid * psz, 64);
-    plan->ws_bytes = align_up(plan->bare_off + psz, 256);
+    red::plan_sizes(n, esz, psz, in == AK_MAT2_MODP, target_blocks, dev.sm_count, plan);
     return AK_OK;
 }
 
@@ -252,7 +27,7 @@ ak_status run_reduce(const ReduceCall& c, const ReducePlan& plan) {
                 using Map = typename decltype(tm)::type;
                 return dispatch_monoid<Op, Acc>(c.no_neutral, [&](auto tmo) -> ak_status {
                     using M = typename decltype(tmo)::type;
-                    return launch<In, Acc, Out, Map, M>(c, plan);
+                    return red::launch<In, Acc, Out, Map, M>(c, plan);
                 });
             });
         });
