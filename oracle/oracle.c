@@ -236,7 +236,9 @@ typedef struct {
     int64_t nout, nfold;
 } dims_plan;
 
-static int make_plan(dims_plan* p, int ndim, const int64_t* shape, uint32_t mask) {
+/* strides: element strides of the source per dimension (a strided view), or
+ * NULL for the dense column-major layout. */
+static int make_plan(dims_plan* p, int ndim, const int64_t* shape, const int64_t* strides, uint32_t mask) {
     if (ndim < 1 || ndim > 16) return -1;
     p->ndim = ndim;
     p->nkept = p->nred = 0;
@@ -245,7 +247,7 @@ static int make_plan(dims_plan* p, int ndim, const int64_t* shape, uint32_t mask
     for (int d = 0; d < ndim; ++d) {
         if (shape[d] < 0) return -1;
         p->shape[d] = shape[d];
-        p->stride[d] = st;
+        p->stride[d] = strides ? strides[d] : st;
         st *= shape[d];
         if (mask & (1u << d)) { p->red[p->nred++] = d; p->nfold *= shape[d]; }
         else { p->kept[p->nkept++] = d; p->nout *= shape[d]; }
@@ -267,8 +269,14 @@ static int64_t offset_of(const dims_plan* p, const int* dims, int nd, int64_t o)
 
 int orc_reduce_dims_float(const void* x, int ndim, const int64_t* shape, uint32_t mask,
                           int in_type, int map, int op, int has_init, double init, double* out) {
+    return orc_reduce_dims_float_s(x, ndim, shape, NULL, mask, in_type, map, op, has_init, init, out);
+}
+
+int orc_reduce_dims_float_s(const void* x, int ndim, const int64_t* shape, const int64_t* strides,
+                            uint32_t mask, int in_type, int map, int op, int has_init, double init,
+                            double* out) {
     dims_plan p;
-    if (make_plan(&p, ndim, shape, mask) || !valid_float_args(in_type, map, op)) return -1;
+    if (make_plan(&p, ndim, shape, strides, mask) || !valid_float_args(in_type, map, op)) return -1;
     if (p.nfold == 0 && !has_init) return 1;
     for (int64_t o = 0; o < p.nout; ++o) {
         int64_t base = offset_of(&p, p.kept, p.nkept, o);
@@ -286,8 +294,14 @@ int orc_reduce_dims_float(const void* x, int ndim, const int64_t* shape, uint32_
 int orc_reduce_dims_int(const void* x, int ndim, const int64_t* shape, uint32_t mask,
                         int in_type, int acc_bits, int map, int op, int has_init, int64_t init,
                         int64_t* out) {
+    return orc_reduce_dims_int_s(x, ndim, shape, NULL, mask, in_type, acc_bits, map, op, has_init, init, out);
+}
+
+int orc_reduce_dims_int_s(const void* x, int ndim, const int64_t* shape, const int64_t* strides,
+                          uint32_t mask, int in_type, int acc_bits, int map, int op, int has_init,
+                          int64_t init, int64_t* out) {
     dims_plan p;
-    if (make_plan(&p, ndim, shape, mask) || !valid_int_args(in_type, acc_bits, map, op)) return -1;
+    if (make_plan(&p, ndim, shape, strides, mask) || !valid_int_args(in_type, acc_bits, map, op)) return -1;
     if (p.nfold == 0 && !has_init) return 1;
     for (int64_t o = 0; o < p.nout; ++o) {
         int64_t base = offset_of(&p, p.kept, p.nkept, o);
@@ -305,8 +319,13 @@ int orc_reduce_dims_int(const void* x, int ndim, const int64_t* shape, uint32_t 
 
 int orc_reduce_dims_mat2(const uint32_t* x, int ndim, const int64_t* shape, uint32_t mask,
                          const uint32_t* init, uint32_t* out) {
+    return orc_reduce_dims_mat2_s(x, ndim, shape, NULL, mask, init, out);
+}
+
+int orc_reduce_dims_mat2_s(const uint32_t* x, int ndim, const int64_t* shape, const int64_t* strides,
+                           uint32_t mask, const uint32_t* init, uint32_t* out) {
     dims_plan p;
-    if (make_plan(&p, ndim, shape, mask)) return -1;
+    if (make_plan(&p, ndim, shape, strides, mask)) return -1;
     if (p.nfold == 0 && !init) return 1;
     for (int64_t o = 0; o < p.nout; ++o) {
         int64_t base = offset_of(&p, p.kept, p.nkept, o);
@@ -416,5 +435,208 @@ int orc_scan_mat2(const uint32_t* x, int ndim, const int64_t* shape, int dim,
             memcpy(y + 4 * k, a, sizeof a);
         }
     }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* exclusive scans                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Exclusive scan along each line: y_1 = init, y_i = op(y_{i-1}, x_{i-1}),
+ * i.e. element i holds the fold of init and every element before it. init
+ * is required: the first output is the empty prefix, which has a value only
+ * through init. */
+int orc_scan_excl_float(const void* x, int ndim, const int64_t* shape, int dim, int in_type, int op,
+                        double init, double* y) {
+    scan_lines s;
+    if (make_lines(&s, ndim, shape, dim) || !valid_float_args(in_type, ORC_MAP_IDENTITY, op)) return -1;
+    if (s.len == 0) return 0;
+    for (int64_t e = 0; e < s.n; ++e) {
+        if (!is_line_start(&s, e)) continue;
+        ffold a;
+        ffold_start(&a, init);
+        for (int64_t j = 0; j < s.len; ++j) {
+            int64_t k = e + j * s.step;
+            y[k] = ffold_value(&a);
+            ffold_step(&a, load_float(x, in_type, k), op);
+        }
+    }
+    return 0;
+}
+
+int orc_scan_excl_int(const void* x, int ndim, const int64_t* shape, int dim, int in_type, int acc_bits,
+                      int op, int64_t init, int64_t* y) {
+    scan_lines s;
+    if (make_lines(&s, ndim, shape, dim) || !valid_int_args(in_type, acc_bits, ORC_MAP_IDENTITY, op))
+        return -1;
+    if (s.len == 0) return 0;
+    for (int64_t e = 0; e < s.n; ++e) {
+        if (!is_line_start(&s, e)) continue;
+        int64_t a = wrap((uint64_t)init, acc_bits);
+        for (int64_t j = 0; j < s.len; ++j) {
+            int64_t k = e + j * s.step;
+            y[k] = a;
+            a = istep(a, wrap((uint64_t)load_int(x, in_type, k), acc_bits), op, acc_bits);
+        }
+    }
+    return 0;
+}
+
+int orc_scan_excl_mat2(const uint32_t* x, int ndim, const int64_t* shape, int dim, const uint32_t* init,
+                       uint32_t* y) {
+    scan_lines s;
+    if (make_lines(&s, ndim, shape, dim) || !init) return -1;
+    if (s.len == 0) return 0;
+    for (int64_t e = 0; e < s.n; ++e) {
+        if (!is_line_start(&s, e)) continue;
+        uint32_t a[4], t[4];
+        memcpy(a, init, sizeof a);
+        for (int64_t j = 0; j < s.len; ++j) {
+            int64_t k = e + j * s.step;
+            memcpy(y + 4 * k, a, sizeof a);
+            orc_mat2_mul(a, x + 4 * k, t);
+            memcpy(a, t, sizeof a);
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* findall                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Indices (0-based, increasing) of the elements that are not zero; returns
+ * their count. Bytes (Bool flags) and integers compare with 0; floats with
+ * 0.0, so -0.0 counts as zero and NaN as not zero. */
+int64_t orc_findall(const void* x, int64_t n, int in_type, int64_t* idx) {
+    if (n < 0) return -1;
+    int64_t c = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        int set;
+        switch (in_type) {
+        case ORC_U8: set = ((const uint8_t*)x)[i] != 0; break;
+        case ORC_I32: set = ((const int32_t*)x)[i] != 0; break;
+        case ORC_I64: set = ((const int64_t*)x)[i] != 0; break;
+        case ORC_F32: set = ((const float*)x)[i] != 0.0f; break;
+        case ORC_F64: set = ((const double*)x)[i] != 0.0; break;
+        default: return -1;
+        }
+        if (set) idx[c++] = i;
+    }
+    return c;
+}
+
+/* ------------------------------------------------------------------------ */
+/* fused two-source reductions: r = op(init, f(x_1, y_1), ..., f(x_n, y_n)) */
+/* ------------------------------------------------------------------------ */
+
+static double fmap2(double a, double b, int map2) {
+    switch (map2) {
+    case ORC_MAP2_MUL: return a * b;
+    case ORC_MAP2_SQDIFF: return (a - b) * (a - b);
+    case ORC_MAP2_ABSDIFF: return fabs(a - b);
+    default: return NAN;
+    }
+}
+
+static int64_t imap2(int64_t a, int64_t b, int map2, int bits) {
+    uint64_t d = (uint64_t)a - (uint64_t)b;
+    switch (map2) {
+    case ORC_MAP2_MUL: return wrap((uint64_t)a * (uint64_t)b, bits);
+    case ORC_MAP2_SQDIFF: return wrap(wrap(d, bits) * (uint64_t)wrap(d, bits), bits);
+    case ORC_MAP2_ABSDIFF: {
+        int64_t w = wrap(d, bits);
+        return wrap(w < 0 ? (uint64_t)0 - (uint64_t)w : (uint64_t)w, bits);
+    }
+    default: return 0;
+    }
+}
+
+int orc_reduce2_float(const void* x, const void* y, int64_t n, int in_type, int map2, int op,
+                      int has_init, double init, double* out) {
+    if (!valid_float_args(in_type, ORC_MAP_IDENTITY, op) || map2 < ORC_MAP2_MUL || map2 > ORC_MAP2_ABSDIFF ||
+        n < 0)
+        return -1;
+    ffold a;
+    int64_t i = 0;
+    if (has_init) ffold_start(&a, init);
+    else if (n > 0) {
+        ffold_start(&a, fmap2(load_float(x, in_type, 0), load_float(y, in_type, 0), map2));
+        i = 1;
+    } else return 1;
+    for (; i < n; ++i) ffold_step(&a, fmap2(load_float(x, in_type, i), load_float(y, in_type, i), map2), op);
+    *out = ffold_value(&a);
+    return 0;
+}
+
+int orc_reduce2_int(const void* x, const void* y, int64_t n, int in_type, int acc_bits, int map2, int op,
+                    int has_init, int64_t init, int64_t* out) {
+    if (!valid_int_args(in_type, acc_bits, ORC_MAP_IDENTITY, op) || map2 < ORC_MAP2_MUL ||
+        map2 > ORC_MAP2_ABSDIFF || n < 0)
+        return -1;
+    int64_t a;
+    int64_t i = 0;
+    if (has_init) a = wrap((uint64_t)init, acc_bits);
+    else if (n > 0) {
+        a = imap2(wrap((uint64_t)load_int(x, in_type, 0), acc_bits), wrap((uint64_t)load_int(y, in_type, 0), acc_bits),
+                  map2, acc_bits);
+        i = 1;
+    } else return 1;
+    for (; i < n; ++i)
+        a = istep(a, imap2(wrap((uint64_t)load_int(x, in_type, i), acc_bits),
+                           wrap((uint64_t)load_int(y, in_type, i), acc_bits), map2, acc_bits), op, acc_bits);
+    *out = a;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* affine maps mod p: the user-defined operator of the template API's tests  */
+/* ------------------------------------------------------------------------ */
+
+/* An element (a, b) is the map v -> a*v + b mod p, entries in [0, p). The
+ * operator composes left to right: op(f, g) applies f first, then g:
+ * g(f(v)) = a_g*(a_f*v + b_f) + b_g, i.e. (a_g*a_f, a_g*b_f + b_g). It is
+ * associative, not commutative, and (1, 0) is its identity. */
+void orc_affine_compose(const uint32_t f[2], const uint32_t g[2], uint32_t out[2]) {
+    const uint64_t p = ORC_MODP;
+    uint64_t a = ((uint64_t)g[0] * f[0]) % p;
+    uint64_t b = ((uint64_t)g[0] * f[1] + g[1]) % p;
+    out[0] = (uint32_t)a;
+    out[1] = (uint32_t)b;
+}
+
+/* Inclusive (exclusive = 0) or exclusive scan of n affine maps with an
+ * optional init on the left (required for the exclusive scan). */
+int orc_scan_affine(const uint32_t* x, int64_t n, const uint32_t* init, int exclusive, uint32_t* y) {
+    if (n < 0 || (exclusive && !init)) return -1;
+    uint32_t a[2], t[2];
+    int64_t i = 0;
+    if (init) memcpy(a, init, sizeof a);
+    else if (n > 0) {
+        memcpy(a, x, sizeof a);
+        memcpy(y, a, sizeof a);
+        i = 1;
+    }
+    for (; i < n; ++i) {
+        if (exclusive) memcpy(y + 2 * i, a, sizeof a);
+        orc_affine_compose(a, x + 2 * i, t);
+        memcpy(a, t, sizeof a);
+        if (!exclusive) memcpy(y + 2 * i, a, sizeof a);
+    }
+    return 0;
+}
+
+int orc_reduce_affine(const uint32_t* x, int64_t n, const uint32_t* init, uint32_t out[2]) {
+    if (n < 0) return -1;
+    uint32_t a[2], t[2];
+    int64_t i = 0;
+    if (init) memcpy(a, init, sizeof a);
+    else if (n > 0) memcpy(a, x + 2 * i++, sizeof a);
+    else return 1;
+    for (; i < n; ++i) {
+        orc_affine_compose(a, x + 2 * i, t);
+        memcpy(a, t, sizeof a);
+    }
+    memcpy(out, a, sizeof a);
     return 0;
 }

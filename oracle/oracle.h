@@ -15,7 +15,12 @@
  *   reduce_dims the same fold per output of a column-major array, over the
  *               reduced indices in increasing column-major order;
  *   scan        y_1 = op(init, x_1) (or x_1), y_i = op(y_{i-1}, x_i), for the
- *               whole array or along one dimension.
+ *               whole array or along one dimension; the exclusive scan
+ *               y_1 = init, y_i = op(y_{i-1}, x_{i-1});
+ *   findall     the indices of the nonzero elements, in order;
+ *   reduce2     the reduce of f(x_i, y_i) over two sources (a fused source);
+ *   affine      scans / reduces of affine maps mod p (the test operator of the
+ *               C++ template API).
  * No neutral element is ever used: every fold starts from init or from the
  * first element, which is the meaning of an operator without one.
  *
@@ -40,9 +45,11 @@
 extern "C" {
 #endif
 
-enum { ORC_F32 = 0, ORC_F64 = 1, ORC_BF16 = 2, ORC_I32 = 3, ORC_I64 = 4, ORC_MAT2 = 5 };
+enum { ORC_F32 = 0, ORC_F64 = 1, ORC_BF16 = 2, ORC_I32 = 3, ORC_I64 = 4, ORC_MAT2 = 5, ORC_U8 = 6 };
 enum { ORC_MAP_IDENTITY = 0, ORC_MAP_ABS = 1, ORC_MAP_ABS2 = 2 };
 enum { ORC_OP_ADD = 0, ORC_OP_MUL = 1, ORC_OP_MAX = 2, ORC_OP_MIN = 3, ORC_OP_MATMUL = 4 };
+/* maps of two sources (fused / Broadcasted sources): x*y, (x-y)^2, |x-y| */
+enum { ORC_MAP2_MUL = 0, ORC_MAP2_SQDIFF = 1, ORC_MAP2_ABSDIFF = 2 };
 
 #define ORC_MODP 2147483647u
 
@@ -74,6 +81,17 @@ int orc_reduce_dims_int(const void* x, int ndim, const int64_t* shape, uint32_t 
                         int64_t* out);
 int orc_reduce_dims_mat2(const uint32_t* x, int ndim, const int64_t* shape, uint32_t dims_mask,
                          const uint32_t* init, uint32_t* out);
+/* The same over a strided view: element (i_1, ..., i_d) of the source sits at
+ * sum_k i_k * strides[k] (elements; strides = NULL is the dense layout). The
+ * output stays dense column-major. */
+int orc_reduce_dims_float_s(const void* x, int ndim, const int64_t* shape, const int64_t* strides,
+                            uint32_t dims_mask, int in_type, int map, int op, int has_init, double init,
+                            double* out);
+int orc_reduce_dims_int_s(const void* x, int ndim, const int64_t* shape, const int64_t* strides,
+                          uint32_t dims_mask, int in_type, int acc_bits, int map, int op, int has_init,
+                          int64_t init, int64_t* out);
+int orc_reduce_dims_mat2_s(const uint32_t* x, int ndim, const int64_t* shape, const int64_t* strides,
+                           uint32_t dims_mask, const uint32_t* init, uint32_t* out);
 
 /* --- inclusive scan, whole array (dim = -1) or along dimension dim -------- */
 int orc_scan_float(const void* x, int ndim, const int64_t* shape, int dim, int in_type, int op,
@@ -82,6 +100,40 @@ int orc_scan_int(const void* x, int ndim, const int64_t* shape, int dim, int in_
                  int op, int has_init, int64_t init, int64_t* y);
 int orc_scan_mat2(const uint32_t* x, int ndim, const int64_t* shape, int dim,
                   const uint32_t* init, uint32_t* y);
+
+/* --- exclusive scan: y_1 = init, y_i = op(y_{i-1}, x_{i-1}) (init required:
+ *     the first output is the empty prefix). The pages describe inclusive
+ *     scans only; this is the plain exclusive counterpart, with init as the
+ *     first output of every line. ------------------------------------------ */
+int orc_scan_excl_float(const void* x, int ndim, const int64_t* shape, int dim, int in_type, int op,
+                        double init, double* y);
+int orc_scan_excl_int(const void* x, int ndim, const int64_t* shape, int dim, int in_type, int acc_bits,
+                      int op, int64_t init, int64_t* y);
+int orc_scan_excl_mat2(const uint32_t* x, int ndim, const int64_t* shape, int dim, const uint32_t* init,
+                       uint32_t* y);
+
+/* --- findall (tile-scan PR #202, ratio table and tests paragraph): the
+ *     0-based indices of the elements that are not zero, in increasing
+ *     order; returns their count (-1: bad argument). in_type: ORC_U8 (Bool
+ *     flags), ORC_I32, ORC_I64, ORC_F32, ORC_F64. ----------------------- */
+int64_t orc_findall(const void* x, int64_t n, int in_type, int64_t* idx);
+
+/* --- fused two-source reduce ("Finish whole-array reductions on the
+ *     device", section "What changes": a single-output reduction of a
+ *     Broadcasted source): r = op(init?, f(x_1, y_1), ..., f(x_n, y_n)) with
+ *     f one of ORC_MAP2_*, computed like orc_reduce_*. --------------------- */
+int orc_reduce2_float(const void* x, const void* y, int64_t n, int in_type, int map2, int op,
+                      int has_init, double init, double* out);
+int orc_reduce2_int(const void* x, const void* y, int64_t n, int in_type, int acc_bits, int map2, int op,
+                    int has_init, int64_t init, int64_t* out);
+
+/* --- affine maps mod p (the user-defined operator of the C++ template API's
+ *     tests): element (a, b) = the map v -> a*v + b mod p; op(f, g) applies f
+ *     then g = (a_g*a_f, a_g*b_f + b_g) mod p. ------------------------------ */
+void orc_affine_compose(const uint32_t f[2], const uint32_t g[2], uint32_t out[2]);
+int orc_scan_affine(const uint32_t* x, int64_t n, const uint32_t* init /* nullable */, int exclusive,
+                    uint32_t* y);
+int orc_reduce_affine(const uint32_t* x, int64_t n, const uint32_t* init /* nullable */, uint32_t out[2]);
 
 #ifdef __cplusplus
 }

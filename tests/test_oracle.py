@@ -522,3 +522,167 @@ def test_float_scan_init_once_at_the_left():
     # f64 product with init: exact powers of two
     p = np.full(20, 2.0)
     assert list(oracle.scan(p, "f64", op="mul", init=3.0)) == [3.0 * 2.0**k for k in range(1, 21)]
+
+
+# --------------------------------------------------------------------------
+# exclusive scans: element i is the fold of init and x_1 .. x_{i-1}
+# --------------------------------------------------------------------------
+
+def test_exclusive_scan_of_ones_closed_form():
+    for kind, dt in (("i64", np.int64), ("i32", np.int32), ("f64", np.float64), ("f32", np.float32)):
+        y = oracle.scan(np.ones(1000, dtype=dt), kind, exclusive=True, init=5)
+        assert list(y) == [5 + i for i in range(1000)]
+
+
+@pytest.mark.parametrize("shape,dim", [((1000,), -1), ((7, 9), 0), ((7, 9), 1), ((3, 4, 5), 1)])
+def test_exclusive_int_scan_matches_numpy(shape, dim):
+    n = int(np.prod(shape))
+    x = synth.uniform_int(n, -(2**20), 2**20, np.int64, stream=60)
+    init = 77
+    y = oracle.scan(x, "i64", shape, dim, exclusive=True, init=init)
+    arr = x.reshape(tuple(reversed(shape))) if dim >= 0 else x
+    ax = len(shape) - 1 - dim if dim >= 0 else 0
+    inc = np.cumsum(arr, axis=ax)
+    ref = np.concatenate([np.zeros_like(np.take(inc, [0], axis=ax)), np.delete(inc, -1, axis=ax)], axis=ax) + init
+    assert np.array_equal(y, ref.ravel())
+    ym = oracle.scan(x, "i64", shape, dim, op="max", exclusive=True, init=-(2**62))
+    incm = np.maximum.accumulate(arr, axis=ax)
+    refm = np.concatenate([np.full_like(np.take(incm, [0], axis=ax), -(2**62)), np.delete(incm, -1, axis=ax)],
+                          axis=ax)
+    assert np.array_equal(ym, refm.ravel())
+
+
+def test_exclusive_float_scan_matches_fsum():
+    x = synth.uniform_f32_pm1(3000, stream=61)
+    xd = list(x.astype(np.float64))
+    y = oracle.scan(x, "f32", exclusive=True, init=0.25)
+    for i in (0, 1, 2, 999, 2999):
+        assert y[i] == math.fsum([0.25] + xd[:i])
+    assert y[0] == 0.25
+
+
+def test_exclusive_mat2_scan_is_the_exact_product_of_the_elements_before():
+    x = synth.mat2_modp(9, stream=62)
+    init = synth.mat2_modp(1, stream=63)[0]
+    y = oracle.scan(x, "mat2", exclusive=True, init=init)
+    assert list(y[0]) == [int(v) for v in init]
+    for i in range(1, 9):
+        assert list(y[i]) == _exact_product([init] + list(x[:i]))
+
+
+# --------------------------------------------------------------------------
+# findall
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind", ["u8", "i32", "i64", "f32", "f64"])
+def test_findall_matches_flatnonzero(kind):
+    n = 10_000
+    w = synth.uniform_int(n, 0, 3, np.int64, stream=64)
+    x = np.where(w == 0, 0, w).astype({"u8": np.uint8, "i32": np.int32, "i64": np.int64, "f32": np.float32,
+                                       "f64": np.float64}[kind])
+    idx = oracle.findall(x, kind)
+    assert np.array_equal(idx, np.flatnonzero(x))
+    assert idx.size == int(np.count_nonzero(x))
+    assert np.all(np.diff(idx) > 0)
+
+
+def test_findall_special_values_and_empty():
+    x = np.array([0.0, -0.0, np.nan, 1.0, -2.0, 0.0], dtype=np.float32)
+    assert list(oracle.findall(x, "f32")) == [2, 3, 4]
+    assert oracle.findall(np.zeros(0, np.uint8), "u8").size == 0
+    assert oracle.findall(np.zeros(7, np.uint8), "u8").size == 0
+    assert list(oracle.findall(np.full(5, 255, np.uint8), "u8")) == [0, 1, 2, 3, 4]
+
+
+# --------------------------------------------------------------------------
+# fused two-source reductions
+# --------------------------------------------------------------------------
+
+def test_reduce2_closed_forms():
+    n = 2000
+    k = np.arange(1, n + 1)
+    for kind, dt in (("i64", np.int64), ("f64", np.float64), ("f32", np.float32)):
+        x = k.astype(dt)
+        y = (n + 1 - k).astype(dt)
+        # sum k (n+1-k) = n(n+1)(n+2)/6
+        assert oracle.reduce2(x, y, kind, "mul") == n * (n + 1) * (n + 2) // 6
+        # (k - (k+1))^2 = 1
+        assert oracle.reduce2(x, (k + 1).astype(dt), kind, "sqdiff") == n
+        # |2k - (n+1)|, summed
+        assert oracle.reduce2(x, y, kind, "absdiff") == sum(abs(2 * int(t) - (n + 1)) for t in k)
+        assert oracle.reduce2(x, y, kind, "mul", op="max") == max(int(t) * (n + 1 - int(t)) for t in k)
+        assert oracle.reduce2(x, y, kind, "mul", init=10) == n * (n + 1) * (n + 2) // 6 + 10
+
+
+def test_reduce2_matches_fsum_and_numpy():
+    x = synth.uniform_f32_pm1(5000, stream=65)
+    y = synth.uniform_f32_pm1(5000, stream=66)
+    xd, yd = x.astype(np.float64), y.astype(np.float64)
+    assert oracle.reduce2(x, y, "f32", "mul") == math.fsum(xd * yd)       # products exact in f64
+    assert oracle.reduce2(x, y, "f32", "sqdiff") == math.fsum((xd - yd) ** 2)
+    xi = synth.uniform_int(5000, -1000, 1000, np.int32, stream=67)
+    yi = synth.uniform_int(5000, -1000, 1000, np.int32, stream=68)
+    assert oracle.reduce2(xi, yi, "i32", "mul") == int(np.dot(xi.astype(np.int64), yi.astype(np.int64)))
+    assert oracle.reduce2(xi, yi, "i32", "absdiff") == int(np.abs(xi.astype(np.int64) - yi).sum())
+    assert oracle.reduce2(np.zeros(0, np.float32), np.zeros(0, np.float32), "f32") is None
+
+
+# --------------------------------------------------------------------------
+# strided views
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dims", [(1,), (0,), (0, 1)])
+def test_reduce_dims_of_a_strided_view_matches_numpy(dims):
+    # a 6 x 5 column-major view into a 10 x 8 buffer, starting at (2, 1)
+    buf = synth.uniform_int(80, -1000, 1000, np.int64, stream=69)
+    base = 2 + 10 * 1
+    shape, strides = (6, 5), (1, 10)
+    flat = buf[base:]
+    got = oracle.reduce_dims(flat, "i64", shape, dims, strides=strides)
+    view = buf.reshape(8, 10)[1:6, 2:8]  # row-major view of the column-major sub-block
+    axes = tuple(1 - d for d in dims)
+    assert np.array_equal(got, view.sum(axis=axes, keepdims=True).ravel())
+    # a transposed view (strides swapped) and a view with a stride-2 inner dimension
+    got_t = oracle.reduce_dims(buf, "i64", (8, 10), (1,), strides=(10, 1))
+    assert np.array_equal(got_t, buf.reshape(8, 10).sum(axis=1))
+    got_2 = oracle.reduce_dims(buf, "i64", (5, 8), (0,), strides=(2, 10))
+    assert np.array_equal(got_2, buf.reshape(8, 10)[:, ::2].sum(axis=1))
+    xf = synth.uniform_f32_pm1(80, stream=70)
+    got_f = oracle.reduce_dims(xf[base:], "f32", shape, (1,), strides=strides)
+    vf = xf.astype(np.float64).reshape(8, 10)[1:6, 2:8]
+    assert list(got_f) == [math.fsum(vf[:, i]) for i in range(6)]
+
+
+# --------------------------------------------------------------------------
+# affine maps mod p (the template API's user operator)
+# --------------------------------------------------------------------------
+
+def test_affine_scan_applied_to_a_value_equals_iteration():
+    n = 500
+    x = np.stack([synth.uniform_int(n, 0, P - 1, np.int64, stream=71),
+                  synth.uniform_int(n, 0, P - 1, np.int64, stream=72)], axis=1).astype(np.uint32)
+    y = oracle.scan_affine(x)
+    v0 = 12345
+    v = v0
+    for i in range(n):
+        v = (int(x[i, 0]) * v + int(x[i, 1])) % P
+        assert (int(y[i, 0]) * v0 + int(y[i, 1])) % P == v
+    assert list(oracle.reduce_affine(x)) == list(y[-1])
+    # composition order matters: the reversed product differs
+    assert list(oracle.reduce_affine(x[::-1].copy())) != list(y[-1])
+
+
+def test_affine_special_cases_and_exclusive():
+    n = 300
+    b = synth.uniform_int(n, 0, P - 1, np.int64, stream=73)
+    x = np.stack([np.ones(n, np.int64), b], axis=1).astype(np.uint32)  # translations: b's prefix sums
+    y = oracle.scan_affine(x)
+    assert np.array_equal(y[:, 1].astype(np.int64), np.cumsum(b) % P) and np.all(y[:, 0] == 1)
+    init = np.array([3, 5], np.uint32)
+    ye = oracle.scan_affine(x, init=init, exclusive=True)
+    assert list(ye[0]) == [3, 5]
+    # element i of the exclusive scan, then x_i, is element i of the inclusive scan with init
+    yi = oracle.scan_affine(x, init=init)
+    for i in range(n):
+        assert list(oracle.affine_compose(ye[i], x[i])) == list(yi[i])
+    assert list(yi[0]) == [3, (5 + int(b[0])) % P]

@@ -38,13 +38,16 @@ MUTANTS = [
     ("no wrap to 32 bits", [("if (bits == 64) {", "if (bits == 64 || bits == 32) {")]),
     ("scan: mat2 init on the right",
      [("if (init) orc_mat2_mul(init, x + 4 * e, a);", "if (init) orc_mat2_mul(x + 4 * e, init, a);")]),
-    ("scan: mat2 operands swapped", [("orc_mat2_mul(a, x + 4 * k, t);", "orc_mat2_mul(x + 4 * k, a, t);")]),
+    ("scan: mat2 operands swapped",
+     [("orc_mat2_mul(a, x + 4 * k, t);\n            memcpy(a, t, sizeof a);\n            memcpy(y + 4 * k",
+       "orc_mat2_mul(x + 4 * k, a, t);\n            memcpy(a, t, sizeof a);\n            memcpy(y + 4 * k")]),
     ("dims: wrong stride of a kept / reduced dimension",
      [("off += (o % p->shape[d]) * p->stride[d];", "off += (o % p->shape[d]) * p->stride[d ? d - 1 : 0];")]),
     ("scan: line stride off by one", [("if (d == dim) st_dim = st;", "if (d == dim) st_dim = st * 1 + (d > 0);")]),
     ("bf16 double rounding through f32", [("float f = (float)q; ", "float f = (float)(float)v; ")]),
     ("reduce: float init dropped",
-     [("    if (has_init) ffold_start(&a, init);\n    else if (n > 0)", "    if (0) ffold_start(&a, init);\n    else if (n > 0)")]),
+     [("    if (has_init) ffold_start(&a, init);\n    else if (n > 0) ffold_start(&a, fmap(",
+       "    if (0) ffold_start(&a, init);\n    else if (n > 0) ffold_start(&a, fmap(")]),
     ("dims: float init dropped",
      [("        if (has_init) ffold_start(&a, init);\n        else ffold_start(&a, fmap(",
        "        if (0) ffold_start(&a, init);\n        else ffold_start(&a, fmap(")]),
@@ -67,11 +70,34 @@ MUTANTS = [
     ("scan: float init dropped",
      [("        if (has_init) {\n            ffold_start(&a, init);", "        if (0) {\n            ffold_start(&a, init);")]),
     ("scan: float init applied to every element",
-     [("ffold_step(&a, load_float(x, in_type, k), op);",
-       "ffold_step(&a, load_float(x, in_type, k) + (has_init ? init : 0.0), op);")]),
+     [("ffold_step(&a, load_float(x, in_type, k), op);\n            y[k] = ffold_value(&a);",
+       "ffold_step(&a, load_float(x, in_type, k) + (has_init ? init : 0.0), op);\n            y[k] = ffold_value(&a);")]),
     ("scan: float line stride off by one",
-     [("            int64_t k = e + j * s.step;\n            ffold_step(&a, load_float",
-       "            int64_t k = e + j * (s.step > 1 ? s.step - 1 : 1);\n            ffold_step(&a, load_float")]),
+     [("            int64_t k = e + j * s.step;\n            ffold_step(&a, load_float(x, in_type, k), op);\n            y[k]",
+       "            int64_t k = e + j * (s.step > 1 ? s.step - 1 : 1);\n"
+       "            ffold_step(&a, load_float(x, in_type, k), op);\n            y[k]")]),
+    ("exclusive int scan stores after the combine",
+     [("            y[k] = a;\n            a = istep(a, wrap((uint64_t)load_int(x, in_type, k), acc_bits), op, acc_bits);",
+       "            a = istep(a, wrap((uint64_t)load_int(x, in_type, k), acc_bits), op, acc_bits);\n            y[k] = a;")]),
+    ("exclusive float scan stores after the combine",
+     [("            y[k] = ffold_value(&a);\n            ffold_step(&a, load_float(x, in_type, k), op);",
+       "            ffold_step(&a, load_float(x, in_type, k), op);\n            y[k] = ffold_value(&a);")]),
+    ("exclusive mat2 scan: operands swapped",
+     [("            memcpy(y + 4 * k, a, sizeof a);\n            orc_mat2_mul(a, x + 4 * k, t);",
+       "            memcpy(y + 4 * k, a, sizeof a);\n            orc_mat2_mul(x + 4 * k, a, t);")]),
+    ("findall: floats selected by sign", [("set = ((const float*)x)[i] != 0.0f;", "set = ((const float*)x)[i] > 0.0f;")]),
+    ("findall: only the byte 1 selected", [("set = ((const uint8_t*)x)[i] != 0;", "set = ((const uint8_t*)x)[i] == 1;")]),
+    ("reduce2: square of the difference dropped",
+     [("case ORC_MAP2_SQDIFF: return (a - b) * (a - b);", "case ORC_MAP2_SQDIFF: return (a - b);")]),
+    ("reduce2: integer product uses one source twice",
+     [("case ORC_MAP2_MUL: return wrap((uint64_t)a * (uint64_t)b, bits);",
+       "case ORC_MAP2_MUL: return wrap((uint64_t)a * (uint64_t)a, bits);")]),
+    ("strided view read as dense", [("p->stride[d] = strides ? strides[d] : st;", "p->stride[d] = st;")]),
+    ("affine maps composed in the wrong order",
+     [("uint64_t b = ((uint64_t)g[0] * f[1] + g[1]) % p;", "uint64_t b = ((uint64_t)f[0] * g[1] + f[1]) % p;")]),
+    ("affine exclusive scan stores the inclusive value",
+     [("if (exclusive) memcpy(y + 2 * i, a, sizeof a);", "if (0) memcpy(y + 2 * i, a, sizeof a);"),
+      ("if (!exclusive) memcpy(y + 2 * i, a, sizeof a);", "memcpy(y + 2 * i, a, sizeof a);")]),
 ]
 
 
