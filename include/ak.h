@@ -80,11 +80,16 @@ typedef enum ak_dtype {
     AK_BF16 = 2,
     AK_I32 = 3,
     AK_I64 = 4,
-    AK_MAT2_MODP = 5
+    AK_MAT2_MODP = 5,
+    AK_U8 = 6  /* bytes (Julia Bool flags): findall input only */
 } ak_dtype;
 
 /* f, applied to each element in the accumulator type before op. */
 typedef enum ak_map { AK_MAP_IDENTITY = 0, AK_MAP_ABS = 1, AK_MAP_ABS2 = 2 } ak_map;
+
+/* f of a fused two-source element (ak_reduce2), in the accumulator type:
+ * a*b, (a-b)^2, |a-b| (integers wrap). */
+typedef enum ak_map2 { AK_MAP2_MUL = 0, AK_MAP2_SQDIFF = 1, AK_MAP2_ABSDIFF = 2 } ak_map2;
 
 typedef enum ak_op {
     AK_OP_ADD = 0,
@@ -122,7 +127,11 @@ typedef struct ak_opts {
     int32_t check;            /* 1: synchronize `stream` before returning and report
                                  device-side failures (AK_ERR_TIMEOUT) */
     int32_t flags;            /* tuning switches, AK_FLAG_* (0 = none) */
-    int64_t wait_limit_ns;    /* bound of each device-side wait of the scan; 0 = 1 s */
+    int32_t exclusive;        /* ak_accumulate: 1 = exclusive scan (see ak_accumulate) */
+    int32_t reserved;         /* must be 0 */
+    int64_t wait_limit_ns;    /* bound of each device-side wait of the scan; 0 = 1 s. Without
+                                 `check` a wait that runs out is not reported by the call
+                                 itself: read it with ak_scan_status */
     int64_t debug_skip_publish_tile; /* fault injection for tests: the scan tile with this
                                  index never publishes its state, so its successors'
                                  bounded waits run out; -1 = off */
@@ -175,6 +184,22 @@ ak_status ak_reduce(const void* src, int64_t n, ak_dtype in, ak_map f, ak_op op,
                     void* workspace, size_t workspace_bytes, const ak_opts* opts, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * ak_reduce2: r = op(f(a[0], b[0]), ..., f(a[n-1], b[n-1])) over two sources
+ * of n elements of `in` read side by side -- a fused (Broadcasted) source such
+ * as sum(x .* y) or sum(abs2.(x .- y)), reduced without materialising the
+ * elementwise array. PR #139, "What changes": a single-output reduction whose
+ * source is a Broadcasted takes the whole-array path. Arguments, workspace
+ * (ak_reduce_workspace_size with the same n, in, acc), store modes and empty
+ * rules are ak_reduce's; f is an ak_map2; matrices are not supported. Sources
+ * whose addresses differ by a multiple of 32 bytes are read with 32-byte
+ * vectors, others element by element.
+ * ------------------------------------------------------------------------- */
+ak_status ak_reduce2(const void* src_a, const void* src_b, int64_t n, ak_dtype in, ak_map2 f, ak_op op,
+                     ak_dtype acc, ak_dtype out, const void* init, ak_store mode, void* dst_dev,
+                     void* dst_host, void* workspace, size_t workspace_bytes, const ak_opts* opts,
+                     void* stream);
+
+/* ---------------------------------------------------------------------------
  * ak_reduce_dims: R[kept index] = op over the reduced dimensions of
  * f(src[...]), folded in increasing column-major order of the reduced
  * indices. PR #176: strided reductions into contiguous outputs take a 2-d
@@ -182,20 +207,28 @@ ak_status ak_reduce(const void* src, int64_t n, ak_dtype in, ak_map f, ak_op op,
  * pass) only when the outputs alone do not fill the device; the middle
  * dimension of a 3-d array is handled as runs of contiguous outputs at the
  * offsets of the other kept dimensions. PR #139: a reduction to a single
- * output over one contiguous range takes the whole-array path.
+ * output over one contiguous range takes the whole-array path; its tests
+ * cover offset views, which strides describe here.
  *
  *   ndim, shape   1 <= ndim <= 8, column-major extents (>= 0)
+ *   strides       element strides of src per dimension (>= 0): a strided
+ *                 view (a sub-array, a transpose, a stepped slice); NULL =
+ *                 dense column-major. Views whose kept innermost dimension
+ *                 has unit stride take the strided / row kernels (16-byte
+ *                 loads when src and the strides are 16-byte multiples);
+ *                 others a general kernel (slower: it walks the reduced
+ *                 indices per thread).
  *   dims_mask     bit d set = dimension d is reduced (bits >= ndim invalid)
- *   dst           device, dense column-major array of `out` with the shape of
- *                 src where reduced extents are 1
+ *   dst           device, DENSE column-major array of `out` with the shape
+ *                 of src where reduced extents are 1
  * Empty reductions (a reduced extent is 0) follow ak_reduce's empty rules.
  * ------------------------------------------------------------------------- */
-ak_status ak_reduce_dims_workspace_size(int ndim, const int64_t* shape, uint32_t dims_mask,
-                                        ak_dtype in, ak_dtype acc, const ak_opts* opts,
-                                        size_t* bytes);
-ak_status ak_reduce_dims(const void* src, int ndim, const int64_t* shape, uint32_t dims_mask,
-                         ak_dtype in, ak_map f, ak_op op, ak_dtype acc, ak_dtype out,
-                         const void* init, ak_store mode, void* dst, void* workspace,
+ak_status ak_reduce_dims_workspace_size(int ndim, const int64_t* shape, const int64_t* strides,
+                                        uint32_t dims_mask, ak_dtype in, ak_dtype acc,
+                                        const ak_opts* opts, size_t* bytes);
+ak_status ak_reduce_dims(const void* src, int ndim, const int64_t* shape, const int64_t* strides,
+                         uint32_t dims_mask, ak_dtype in, ak_map f, ak_op op, ak_dtype acc,
+                         ak_dtype out, const void* init, ak_store mode, void* dst, void* workspace,
                          size_t workspace_bytes, const ak_opts* opts, void* stream);
 
 /* ---------------------------------------------------------------------------
@@ -214,9 +247,17 @@ ak_status ak_reduce_dims(const void* src, int ndim, const int64_t* shape, uint32
  *
  *   src, dst      device, same shape; dst may equal src (in place) but must
  *                 not otherwise overlap it
+ * Exclusive scan (opts->exclusive = 1): element i holds the fold of init and
+ *   the elements before it, y_1 = init, y_i = op(y_{i-1}, x_{i-1}). The pages
+ *   describe inclusive scans only; this is its plain exclusive counterpart.
+ *   Without init the neutral element stands for it (0 for +, 1 for *, the
+ *   identity matrix); max / min and no_neutral then fail with
+ *   AK_ERR_EMPTY_NO_INIT, since the first output has no value.
  * A wait that runs out (only possible through debug_skip_publish_tile or a
  * hardware fault) stops the kernel early; with opts->check set the call then
- * returns AK_ERR_TIMEOUT and dst is unspecified.
+ * returns AK_ERR_TIMEOUT and dst is unspecified. Without check the call
+ * returns AK_OK and the failure is recorded in the workspace: after the
+ * stream has reached the end of the call, ak_scan_status(workspace) tells.
  * ------------------------------------------------------------------------- */
 ak_status ak_accumulate_workspace_size(int ndim, const int64_t* shape, int dim, ak_dtype in,
                                        ak_dtype acc, ak_op op, const ak_opts* opts,
@@ -225,6 +266,36 @@ ak_status ak_accumulate(const void* src, void* dst, int ndim, const int64_t* sha
                         ak_dtype in, ak_op op, ak_dtype acc, ak_dtype out, const void* init,
                         void* workspace, size_t workspace_bytes, const ak_opts* opts,
                         void* stream);
+/* Outcome of the last ak_accumulate that used this workspace: AK_OK, or
+ * AK_ERR_TIMEOUT when one of its bounded waits ran out. A blocking read of
+ * the workspace's first word: call it once the caller's stream has passed the
+ * scan (e.g. after cudaStreamSynchronize), not while it runs. */
+ak_status ak_scan_status(const void* workspace);
+
+/* ---------------------------------------------------------------------------
+ * ak_findall: the indices of the nonzero elements of src, in increasing
+ * order, and their count (Julia's findall over a Bool array, or over
+ * x .!= 0). The tile-scan PR #202 counts findall among its scans (ratio
+ * table; its tests paragraph): the output slot of a selected element is the
+ * exclusive count of the selected elements before it. One pass: tiles count
+ * their selected elements, publish the counts and derive their output
+ * offsets by decoupled look-back (bounded waits), then store the indices.
+ *
+ *   src        device, n elements of `in`: AK_U8 (nonzero byte = true),
+ *              AK_I32, AK_I64 (!= 0), AK_F32, AK_F64 (!= 0.0: -0.0 is
+ *              false, NaN true)
+ *   idx        device, room for n int64 (the count is at most n); receives
+ *              the 0-based indices; entries past the count are untouched
+ *   count_dev  device, one int64, or NULL
+ *   count_host host, one int64, or NULL; when given the call synchronizes
+ *              `stream` and returns the count there
+ *   At least one of count_dev / count_host must be non-NULL.
+ * The workspace is cleared by the call on its stream (graph-replay safe).
+ * ------------------------------------------------------------------------- */
+ak_status ak_findall_workspace_size(int64_t n, ak_dtype in, const ak_opts* opts, size_t* bytes);
+ak_status ak_findall(const void* src, int64_t n, ak_dtype in, int64_t* idx, int64_t* count_dev,
+                     int64_t* count_host, void* workspace, size_t workspace_bytes, const ak_opts* opts,
+                     void* stream);
 
 /* ---------------------------------------------------------------------------
  * ak_reduce_noalloc: ak_reduce for callers that cannot allocate device memory.
@@ -245,7 +316,10 @@ ak_status ak_accumulate(const void* src, void* dst, int ndim, const int64_t* sha
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture. Every call on a device shares the one array:
+ * before any stream capture. The address is kept per device and CUDA
+ * context: after a cudaDeviceReset the device's new context holds the array
+ * at a new address, and the next call (again: outside any capture) looks it
+ * up anew. Every call on a device shares the one array:
  * calls that may overlap on the GPU (different streams, no ordering) race
  * on it and give wrong results; order them on one stream. Nothing in the
  * array needs clearing between calls.

@@ -19,16 +19,17 @@ import numpy as np
 import torch
 
 from . import _abi
-from ._abi import DTYPES, MAPS, OPS, SHAPES, STORES
+from ._abi import DTYPES, MAPS, MAPS2, OPS, SHAPES, STORES
 
-__all__ = ["AkError", "ak_reduce", "ak_reduce_dims", "ak_accumulate", "ak_reduce_workspace_size",
+__all__ = ["AkError", "ak_reduce", "ak_reduce2", "ak_reduce_dims", "ak_accumulate", "ak_reduce_workspace_size",
            "ak_reduce_dims_workspace_size", "ak_accumulate_workspace_size", "ak_status_string",
-           "ak_kernel_launch_count", "ak_dims_select", "make_opts", "lib"]
+           "ak_kernel_launch_count", "ak_dims_select", "ak_scan_status", "ak_findall",
+           "ak_findall_workspace_size", "make_opts", "lib"]
 
 _TORCH = {torch.float32: "f32", torch.float64: "f64", torch.bfloat16: "bf16", torch.int32: "i32",
-          torch.int64: "i64"}
+          torch.int64: "i64", torch.uint8: "u8", torch.bool: "u8"}
 _TORCH_OF = {"f32": torch.float32, "f64": torch.float64, "bf16": torch.bfloat16, "i32": torch.int32,
-             "i64": torch.int64, "mat2": torch.int32}
+             "i64": torch.int64, "mat2": torch.int32, "u8": torch.uint8}
 _NP_OF = {"f32": np.float32, "f64": np.float64, "i32": np.int32, "i64": np.int64}
 _DEFAULT_ACC = {"f32": "f32", "f64": "f64", "bf16": "f32", "i32": "i32", "i64": "i64", "mat2": "mat2"}
 
@@ -60,7 +61,7 @@ def ak_kernel_launch_count() -> int:
 
 
 def make_opts(no_neutral=False, target_blocks=0, items_per_thread=0, dims_shape="auto", check=False,
-              wait_limit_ns=0, debug_skip_publish_tile=-1, dims_cluster=False) -> _abi.ak_opts:
+              wait_limit_ns=0, debug_skip_publish_tile=-1, dims_cluster=False, exclusive=False) -> _abi.ak_opts:
     o = _abi.ak_opts()
     lib().ak_opts_default(ctypes.byref(o))
     o.no_neutral = int(bool(no_neutral))
@@ -71,6 +72,7 @@ def make_opts(no_neutral=False, target_blocks=0, items_per_thread=0, dims_shape=
     o.wait_limit_ns = int(wait_limit_ns)
     o.debug_skip_publish_tile = int(debug_skip_publish_tile)
     o.flags = _abi.FLAG_DIMS_CLUSTER if dims_cluster else 0
+    o.exclusive = int(bool(exclusive))
     return o
 
 
@@ -173,6 +175,21 @@ def ak_reduce(src: torch.Tensor, *, f: str = "identity", op: str = "add", acc: s
     host-only fold). Default: 'init' when ``init`` is given, else
     'overwrite'.
     """
+    if src.is_cuda and not src.is_contiguous():
+        # a strided view: all of its dimensions through ak_reduce_dims
+        kind = _kind(src, elem)
+        sh, _ = _view_of(src, kind, None, None)
+        r = dst if dst is not None else torch.empty(4 if (out or acc or _DEFAULT_ACC[kind]) == "mat2" else 1,
+                                                    dtype=_TORCH_OF[out or acc or _DEFAULT_ACC[kind]],
+                                                    device=src.device)
+        if to_host and host_old is not None and mode == "fold":
+            r.fill_(host_old)
+        ak_reduce_dims(src, list(range(len(sh))), f=f, op=op, acc=acc, out=out, init=init, mode=mode, dst=r,
+                       elem=elem, workspace=workspace, opts=opts, stream=stream)
+        if to_host:
+            v = r.cpu()
+            return tuple(int(t) for t in v.view(torch.int32).numpy().view("uint32")) if v.numel() == 4 else v.item()
+        return r
     _require_cuda(src, dst)
     kind = _kind(src, elem)
     acc = acc or _DEFAULT_ACC[kind]
@@ -196,6 +213,37 @@ def ak_reduce(src: torch.Tensor, *, f: str = "identity", op: str = "add", acc: s
     return dst
 
 
+def ak_reduce2(a: torch.Tensor, b: torch.Tensor, *, f: str = "mul", op: str = "add", acc: str | None = None,
+               out: str | None = None, init=None, mode: str | None = None, dst: torch.Tensor | None = None,
+               to_host: bool = False, host_old=None, workspace=None, opts=None, stream=None):
+    """Whole-array mapreduce of a fused two-source element,
+    ``op(f(a_1, b_1), ..., f(a_n, b_n))`` with f 'mul' (a*b), 'sqdiff'
+    ((a-b)^2) or 'absdiff' (|a-b|); a and b have the same dtype and size.
+    Stores and returns like ak_reduce."""
+    _require_cuda(a, b, dst)
+    kind = _kind(a, None)
+    if _kind(b, None) != kind or a.numel() != b.numel():
+        raise ValueError("both sources need the same dtype and number of elements")
+    acc = acc or _DEFAULT_ACC[kind]
+    out = out or acc
+    mode = mode or ("init" if init is not None else "overwrite")
+    n = a.numel()
+    size = ak_reduce_workspace_size(n, kind, acc, opts)
+    wp, wb, _keep = _workspace(size, a.device, workspace)
+    hb = None
+    if to_host:
+        hb = ctypes.create_string_buffer(16)
+        if host_old is not None:
+            ctypes.memmove(hb, _value_bytes(host_old, out if out != "bf16" else "f32"), 16)
+    _check(lib().ak_reduce2(a.data_ptr() if n else None, b.data_ptr() if n else None, n, DTYPES[kind], MAPS2[f],
+                            OPS[op], DTYPES[acc], DTYPES[out], _value_bytes(init, acc), STORES[mode],
+                            dst.data_ptr() if dst is not None else None, hb, wp, wb, _opts_ptr(opts),
+                            _stream(stream)), "ak_reduce2")
+    if to_host:
+        return _from_bytes(hb, out)
+    return dst
+
+
 # ---------------------------------------------------------------------------
 # ak_reduce_dims
 # ---------------------------------------------------------------------------
@@ -207,30 +255,53 @@ def _mask(dims) -> int:
     return m
 
 
-def ak_reduce_dims_workspace_size(shape, dims, in_kind: str, acc: str, opts=None) -> int:
+def ak_reduce_dims_workspace_size(shape, dims, in_kind: str, acc: str, opts=None, strides=None) -> int:
     sh = (ctypes.c_int64 * len(shape))(*shape)
+    st = None if strides is None else (ctypes.c_int64 * len(strides))(*strides)
     b = ctypes.c_size_t()
-    _check(lib().ak_reduce_dims_workspace_size(len(shape), sh, _mask(dims), DTYPES[in_kind], DTYPES[acc],
+    _check(lib().ak_reduce_dims_workspace_size(len(shape), sh, st, _mask(dims), DTYPES[in_kind], DTYPES[acc],
                                                _opts_ptr(opts), ctypes.byref(b)), "ak_reduce_dims_workspace_size")
     return b.value
+
+
+def _view_of(t: torch.Tensor, kind: str, shape, strides):
+    """Column-major shape and element strides of a (possibly non-contiguous)
+    tensor; None strides for a contiguous one."""
+    if shape is not None:
+        return [int(v) for v in shape], (None if strides is None else [int(v) for v in strides])
+    if t.is_contiguous():
+        return _colmajor_shape(t, kind, None), None
+    if kind == "mat2":
+        if t.stride(-1) != 1:
+            raise ValueError("a view of 2x2 matrices must keep each matrix's four entries together")
+        dims, sts = list(t.shape[:-1]), [s // 4 for s in t.stride()[:-1]]
+        if any(s % 4 for s in t.stride()[:-1]):
+            raise ValueError("a view of 2x2 matrices must step by whole matrices")
+    else:
+        dims, sts = list(t.shape), list(t.stride())
+    return [int(v) for v in reversed(dims)] or [1], [int(v) for v in reversed(sts)] or [1]
 
 
 def ak_reduce_dims(src: torch.Tensor, dims, *, shape=None, f: str = "identity", op: str = "add",
                    acc: str | None = None, out: str | None = None, init=None, mode: str | None = None,
                    dst: torch.Tensor | None = None, elem: str | None = None, workspace=None, opts=None,
-                   stream=None) -> torch.Tensor:
+                   stream=None, strides=None) -> torch.Tensor:
     """mapreducedim!: reduce the 0-based column-major dimensions ``dims``.
 
-    Returns ``dst``: a contiguous tensor holding the column-major result
-    (reduced extents 1); allocated when not given, with the row-major shape
-    of the reversed column-major result shape.
+    ``src`` may be a non-contiguous view (a slice, a transpose): its strides
+    are passed to the library, nothing is copied. Returns ``dst``: a
+    contiguous tensor holding the column-major result (reduced extents 1);
+    allocated when not given, with the row-major shape of the reversed
+    column-major result shape.
     """
-    _require_cuda(src, dst)
+    if src is not None and (not src.is_cuda):
+        raise ValueError("arrays must be CUDA tensors")
+    _require_cuda(dst)
     kind = _kind(src, elem)
     acc = acc or _DEFAULT_ACC[kind]
     out = out or (kind if kind == "bf16" else acc)
     mode = mode or ("init" if init is not None else "overwrite")
-    sh = _colmajor_shape(src, kind, shape)
+    sh, st = _view_of(src, kind, shape, strides)
     mask = _mask(dims)
     out_shape = [1 if (mask >> d) & 1 else s for d, s in enumerate(sh)]
     if dst is None:
@@ -238,10 +309,12 @@ def ak_reduce_dims(src: torch.Tensor, dims, *, shape=None, f: str = "identity", 
         if out == "mat2":
             rows = rows + [4]
         dst = torch.empty(rows, dtype=_TORCH_OF[out], device=src.device)
-    size = ak_reduce_dims_workspace_size(sh, dims, kind, acc, opts)
+    size = ak_reduce_dims_workspace_size(sh, dims, kind, acc, opts, strides=st)
     wp, wb, _keep = _workspace(size, src.device, workspace)
     csh = (ctypes.c_int64 * len(sh))(*sh)
-    _check(lib().ak_reduce_dims(src.data_ptr() if src.numel() else None, len(sh), csh, mask, DTYPES[kind], MAPS[f],
+    cst = None if st is None else (ctypes.c_int64 * len(st))(*st)
+    _check(lib().ak_reduce_dims(src.data_ptr() if src.numel() else None, len(sh), csh, cst, mask, DTYPES[kind],
+                                MAPS[f],
                                 OPS[op], DTYPES[acc], DTYPES[out], _value_bytes(init, acc), STORES[mode],
                                 dst.data_ptr() if dst.numel() else None, wp, wb, _opts_ptr(opts),
                                 _stream(stream)), "ak_reduce_dims")
@@ -262,9 +335,18 @@ def ak_accumulate_workspace_size(shape, dim: int, in_kind: str, acc: str, op: st
 
 def ak_accumulate(src: torch.Tensor, *, dim: int = -1, shape=None, op: str = "add", acc: str | None = None,
                   out: str | None = None, init=None, dst: torch.Tensor | None = None, elem: str | None = None,
-                  workspace=None, opts=None, stream=None) -> torch.Tensor:
+                  workspace=None, opts=None, stream=None, exclusive: bool = False) -> torch.Tensor:
     """Inclusive scan (accumulate!): the whole array (dim=-1) or along the
-    0-based column-major dimension ``dim``. ``dst`` may be ``src``."""
+    0-based column-major dimension ``dim``. ``dst`` may be ``src``. With
+    ``exclusive`` element i holds the fold of init (or the neutral element)
+    and the elements before it."""
+    if exclusive:
+        if opts is None:
+            opts = make_opts(exclusive=True)
+        elif isinstance(opts, dict):
+            opts = make_opts(**dict(opts, exclusive=True))
+        else:
+            opts.exclusive = 1
     _require_cuda(src, dst)
     kind = _kind(src, elem)
     acc = acc or _DEFAULT_ACC[kind]
@@ -281,6 +363,50 @@ def ak_accumulate(src: torch.Tensor, *, dim: int = -1, shape=None, op: str = "ad
                                _value_bytes(init, acc), wp, wb, _opts_ptr(opts), _stream(stream)),
            "ak_accumulate")
     return dst
+
+
+# ---------------------------------------------------------------------------
+# ak_findall
+# ---------------------------------------------------------------------------
+
+def ak_findall_workspace_size(n: int, in_kind: str, opts=None) -> int:
+    b = ctypes.c_size_t()
+    _check(lib().ak_findall_workspace_size(int(n), DTYPES[in_kind], _opts_ptr(opts), ctypes.byref(b)),
+           "ak_findall_workspace_size")
+    return b.value
+
+
+def ak_findall(src: torch.Tensor, *, idx: torch.Tensor | None = None, count: torch.Tensor | None = None,
+               to_host: bool = True, workspace=None, opts=None, stream=None):
+    """Indices (0-based, increasing, int64) of the nonzero elements of src
+    (bool / uint8 flags, int32, int64, float32, float64). With ``to_host``
+    returns ``idx[:count]`` (the call synchronizes); otherwise returns
+    ``(idx, count)`` with the count in a one-element device tensor."""
+    _require_cuda(src, idx, count)
+    kind = _kind(src, None)
+    if kind not in ("u8", "i32", "i64", "f32", "f64"):
+        raise ValueError("findall takes bool / uint8, int32, int64, float32 or float64 arrays")
+    n = src.numel()
+    if idx is None:
+        idx = torch.empty(max(n, 1), dtype=torch.int64, device=src.device)
+    if not to_host and count is None:
+        count = torch.empty(1, dtype=torch.int64, device=src.device)
+    size = ak_findall_workspace_size(n, kind, opts)
+    wp, wb, _keep = _workspace(size, src.device, workspace)
+    hc = ctypes.c_int64(-1) if to_host else None
+    _check(lib().ak_findall(src.data_ptr() if n else None, n, DTYPES[kind], idx.data_ptr(),
+                            count.data_ptr() if count is not None else None,
+                            ctypes.byref(hc) if hc is not None else None, wp, wb, _opts_ptr(opts),
+                            _stream(stream)), "ak_findall")
+    if to_host:
+        return idx[: hc.value]
+    return idx, count
+
+
+def ak_scan_status(workspace: torch.Tensor) -> int:
+    """Status of the last ak_accumulate on this workspace (0 ok, AK_ERR_TIMEOUT
+    when a bounded wait ran out); call after the stream has passed the scan."""
+    return int(lib().ak_scan_status(workspace.data_ptr()))
 
 
 def ak_dims_select(inner: int, red_len: int, outer: int, elem_bytes: int, vec_elems: int, sm_count: int,

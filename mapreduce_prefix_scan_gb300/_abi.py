@@ -14,8 +14,9 @@ LIB_PATH = os.path.join(_HERE, "_build", "libak.so")
 # enums of include/ak.h
 AK_OK, AK_ERR_INVALID_ARG, AK_ERR_UNSUPPORTED, AK_ERR_WORKSPACE, AK_ERR_EMPTY_NO_INIT, AK_ERR_CUDA, \
     AK_ERR_TIMEOUT = range(7)
-DTYPES = {"f32": 0, "f64": 1, "bf16": 2, "i32": 3, "i64": 4, "mat2": 5}
+DTYPES = {"f32": 0, "f64": 1, "bf16": 2, "i32": 3, "i64": 4, "mat2": 5, "u8": 6}
 MAPS = {"identity": 0, "abs": 1, "abs2": 2}
+MAPS2 = {"mul": 0, "sqdiff": 1, "absdiff": 2}
 OPS = {"add": 0, "mul": 1, "max": 2, "min": 3, "matmul": 4}
 STORES = {"overwrite": 0, "init": 1, "fold": 2}
 SHAPES = {"auto": 0, "thread": 1, "tiled": 2, "columns": 3}
@@ -23,15 +24,17 @@ FLAG_DIMS_CLUSTER = 1
 
 # every symbol include/ak.h declares
 EXPORTS = ("ak_opts_default", "ak_status_string", "ak_dtype_size", "ak_last_cuda_error",
-           "ak_kernel_launch_count", "ak_reduce_workspace_size", "ak_reduce",
+           "ak_kernel_launch_count", "ak_reduce_workspace_size", "ak_reduce", "ak_reduce2",
            "ak_reduce_dims_workspace_size", "ak_reduce_dims", "ak_accumulate_workspace_size",
-           "ak_accumulate", "ak_dims_select", "ak_reduce_noalloc")
+           "ak_accumulate", "ak_scan_status", "ak_findall_workspace_size", "ak_findall", "ak_dims_select",
+           "ak_reduce_noalloc")
 
 
 class ak_opts(ctypes.Structure):
     _fields_ = [("no_neutral", ctypes.c_int32), ("target_blocks", ctypes.c_int32),
                 ("items_per_thread", ctypes.c_int32), ("dims_shape", ctypes.c_int32),
                 ("check", ctypes.c_int32), ("flags", ctypes.c_int32),
+                ("exclusive", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("wait_limit_ns", ctypes.c_int64), ("debug_skip_publish_tile", ctypes.c_int64)]
 
 
@@ -67,14 +70,19 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.ak_kernel_launch_count.restype = ctypes.c_uint64
     L.ak_reduce_workspace_size.argtypes = [I64, I32, I32, PO, PSZ]
     L.ak_reduce.argtypes = [P, I64, I32, I32, I32, I32, I32, P, I32, P, P, P, SZ, PO, P]
-    L.ak_reduce_dims_workspace_size.argtypes = [I32, PI64, U32, I32, I32, PO, PSZ]
-    L.ak_reduce_dims.argtypes = [P, I32, PI64, U32, I32, I32, I32, I32, I32, P, I32, P, P, SZ, PO, P]
+    L.ak_reduce2.argtypes = [P, P, I64, I32, I32, I32, I32, I32, P, I32, P, P, P, SZ, PO, P]
+    L.ak_reduce_dims_workspace_size.argtypes = [I32, PI64, PI64, U32, I32, I32, PO, PSZ]
+    L.ak_reduce_dims.argtypes = [P, I32, PI64, PI64, U32, I32, I32, I32, I32, I32, P, I32, P, P, SZ, PO, P]
     L.ak_accumulate_workspace_size.argtypes = [I32, PI64, I32, I32, I32, I32, PO, PSZ]
     L.ak_accumulate.argtypes = [P, P, I32, PI64, I32, I32, I32, I32, I32, P, P, SZ, PO, P]
+    L.ak_scan_status.argtypes = [P]
+    L.ak_findall_workspace_size.argtypes = [I64, I32, PO, PSZ]
+    L.ak_findall.argtypes = [P, I64, I32, P, P, P, P, SZ, PO, P]
     L.ak_dims_select.argtypes = [I64, I64, I64, I32, I32, I32, I32, PI32, PI32, PI32, PI32]
     L.ak_reduce_noalloc.argtypes = [P, I64, I32, I32, I32, I32, I32, P, I32, P, P, PO, P]
-    for f in ("ak_reduce_workspace_size", "ak_reduce", "ak_reduce_dims_workspace_size", "ak_reduce_dims",
-              "ak_accumulate_workspace_size", "ak_accumulate", "ak_dims_select", "ak_reduce_noalloc"):
+    for f in ("ak_reduce_workspace_size", "ak_reduce", "ak_reduce2", "ak_reduce_dims_workspace_size", "ak_reduce_dims",
+              "ak_accumulate_workspace_size", "ak_accumulate", "ak_scan_status", "ak_findall_workspace_size",
+              "ak_findall", "ak_dims_select", "ak_reduce_noalloc"):
         getattr(L, f).restype = I32
     if path == LIB_PATH:
         _lib = L

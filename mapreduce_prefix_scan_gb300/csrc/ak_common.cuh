@@ -145,6 +145,18 @@ __device__ __forceinline__ T shfl_down_any(const T& v, int d) {
     return r;
 }
 
+// shfl_down within segments of `width` lanes (a power of two <= 32).
+template <class T>
+__device__ __forceinline__ T shfl_down_width(const T& v, int d, int width) {
+    static_assert(sizeof(T) % 4 == 0, "word-sized types only");
+    T r;
+    const uint32_t* s = reinterpret_cast<const uint32_t*>(&v);
+    uint32_t* o = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(T) / 4); ++i) o[i] = __shfl_down_sync(0xffffffffu, s[i], d, width);
+    return r;
+}
+
 template <class T>
 __device__ __forceinline__ T shfl_up_any(const T& v, int d) {
     T r;

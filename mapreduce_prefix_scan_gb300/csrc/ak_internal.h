@@ -45,7 +45,7 @@ inline ak_status check_launch() {
 
 // Workspace header (first 256 bytes of every workspace).
 struct WsHeader {
-    uint64_t error_word;  // (epoch << 8) | code, written by a kernel that gave up waiting
+    uint64_t error_word;  // the call's epoch, written by a kernel that gave up waiting
     uint64_t pad[31];
 };
 constexpr size_t kWsHeader = 256;
@@ -131,6 +131,8 @@ struct alignas(16) Value16 {
 
 struct ReduceCall {
     const void* src;
+    const void* src2;  // second source of a fused element f(src[i], src2[i]), or NULL
+    int map2;          // ak_map2 of the fused element
     int64_t n;  // > 0
     ak_dtype in, acc, out;
     ak_map f;
@@ -156,10 +158,12 @@ ak_status plan_reduce(int64_t n, ak_dtype in, ak_dtype acc, bool no_neutral, int
                       const DeviceInfo& dev, ReducePlan* plan);
 ak_status run_reduce(const ReduceCall& c, const ReducePlan& plan);
 
-// Canonical strided problem: out[i + inner*k] = fold_j x[i + inner*(j + red*k)].
+// Canonical strided problem: out[i + inner*k] = fold_j x[i + ldj*j + ldk*k]
+// (a dense array has ldj = inner, ldk = inner*red).
 struct DimsCall {
     const void* src;
     int64_t inner, red, outer;
+    int64_t ldj, ldk;  // source strides (elements) of the reduced and of the outer dimension
     ak_dtype in, acc, out;
     ak_map f;
     ak_op op;
@@ -173,9 +177,10 @@ struct DimsCall {
     bool allow_cluster;  // AK_FLAG_DIMS_CLUSTER: combine split blocks in a cluster whenever one fits
     bool auto_cluster;   // auto shape: combine in a cluster for small inputs (see select_shape)
     cudaStream_t stream;
-    // general fallback (any dims mask): full shape and mask
+    // general fallback (any dims mask, any strides): full shape, strides and mask
     int ndim;
     int64_t shape[8];
+    int64_t stride[8];
     uint32_t mask;
     bool general;
 };
@@ -202,6 +207,7 @@ struct ScanCall {
     ak_op op;
     bool no_neutral;
     bool has_init;
+    bool exclusive;  // element i = fold of init and the elements before it (has_init is then set)
     Value16 init;
     void* ws;
     size_t ws_bytes;
@@ -230,5 +236,11 @@ ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_d
                     ak_op op, bool no_neutral, int target_blocks, int items,
                     const DeviceInfo& dev, ScanPlan* plan);
 ak_status run_scan(const ScanCall& c, const ScanPlan& plan);
+
+// findall: tiles and workspace; the kernel of findall.cu.
+ak_status plan_findall(int64_t n, ak_dtype in, int64_t* ntiles, size_t* ws_bytes, size_t* count_off);
+ak_status run_findall(const void* src, int64_t n, ak_dtype in, int64_t* idx, int64_t* count, void* ws,
+                      int64_t ntiles, size_t ws_bytes, uint64_t epoch, int64_t wait_limit_ns, int64_t skip_tile,
+                      int target_blocks, cudaStream_t stream);
 
 }  // namespace ak

@@ -105,6 +105,32 @@ struct MapAbs2 {
     static AK_HD int64_t apply(int64_t x) { return wmul(x, x); }
 };
 
+// maps f(a, b) of a fused two-source element (a Broadcasted source such as
+// x .* y or abs2.(x .- y)), applied in the accumulator type; integers wrap
+AK_HD int32_t wsub(int32_t a, int32_t b) { return (int32_t)((uint32_t)a - (uint32_t)b); }
+AK_HD int64_t wsub(int64_t a, int64_t b) { return (int64_t)((uint64_t)a - (uint64_t)b); }
+
+struct Map2Mul {
+    static AK_HD float apply(float a, float b) { return a * b; }
+    static AK_HD double apply(double a, double b) { return a * b; }
+    static AK_HD int32_t apply(int32_t a, int32_t b) { return wmul(a, b); }
+    static AK_HD int64_t apply(int64_t a, int64_t b) { return wmul(a, b); }
+};
+
+struct Map2SqDiff {
+    static AK_HD float apply(float a, float b) { const float d = a - b; return d * d; }
+    static AK_HD double apply(double a, double b) { const double d = a - b; return d * d; }
+    static AK_HD int32_t apply(int32_t a, int32_t b) { const int32_t d = wsub(a, b); return wmul(d, d); }
+    static AK_HD int64_t apply(int64_t a, int64_t b) { const int64_t d = wsub(a, b); return wmul(d, d); }
+};
+
+struct Map2AbsDiff {
+    static AK_HD float apply(float a, float b) { return fabsf(a - b); }
+    static AK_HD double apply(double a, double b) { return fabs(a - b); }
+    static AK_HD int32_t apply(int32_t a, int32_t b) { const int32_t d = wsub(a, b); return d < 0 ? wneg(d) : d; }
+    static AK_HD int64_t apply(int64_t a, int64_t b) { const int64_t d = wsub(a, b); return d < 0 ? wneg(d) : d; }
+};
+
 // --------------------------------------------------------------------------
 // operators
 // --------------------------------------------------------------------------

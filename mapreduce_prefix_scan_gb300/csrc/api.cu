@@ -80,7 +80,7 @@ size_t partial_size(ak_dtype acc, bool no_neutral) {
 // validation helpers
 // ---------------------------------------------------------------------------
 
-static bool valid_dtype(int t) { return t >= AK_F32 && t <= AK_MAT2_MODP; }
+static bool valid_dtype(int t) { return t >= AK_F32 && t <= AK_U8; }
 
 static ak_status check_types(ak_dtype in, ak_map f, ak_op op, ak_dtype acc, ak_dtype out) {
     if (!valid_dtype(in) || !valid_dtype(acc) || !valid_dtype(out)) return AK_ERR_INVALID_ARG;
@@ -212,6 +212,7 @@ extern "C" size_t ak_dtype_size(ak_dtype t) {
     case AK_I32: return 4;
     case AK_I64: return 8;
     case AK_MAT2_MODP: return 16;
+    case AK_U8: return 1;
     default: return 0;
     }
 }
@@ -237,12 +238,18 @@ extern "C" ak_status ak_reduce_workspace_size(int64_t n, ak_dtype in, ak_dtype a
     return AK_OK;
 }
 
-extern "C" ak_status ak_reduce(const void* src, int64_t n, ak_dtype in, ak_map f, ak_op op, ak_dtype acc,
-                               ak_dtype out, const void* init, ak_store mode, void* dst_dev, void* dst_host,
-                               void* ws, size_t ws_bytes, const ak_opts* opts, void* stream) {
+// ak_reduce and ak_reduce2: one source, or a fused element f(src[i], src2[i]).
+static ak_status reduce_impl(const void* src, const void* src2, int map2, int64_t n, ak_dtype in, ak_map f,
+                             ak_op op, ak_dtype acc, ak_dtype out, const void* init, ak_store mode, void* dst_dev,
+                             void* dst_host, void* ws, size_t ws_bytes, const ak_opts* opts, void* stream) {
     ak_status s = check_types(in, f, op, acc, out);
     if (s != AK_OK) return s;
     if (n < 0 || (n > 0 && !src) || (!dst_dev && !dst_host)) return AK_ERR_INVALID_ARG;
+    if (src2) {
+        if (map2 < AK_MAP2_MUL || map2 > AK_MAP2_ABSDIFF || f != AK_MAP_IDENTITY) return AK_ERR_INVALID_ARG;
+        if (in == AK_MAT2_MODP) return AK_ERR_UNSUPPORTED;
+        if (!aligned(src2, ak_dtype_size(in))) return AK_ERR_INVALID_ARG;
+    }
     if (mode < AK_STORE_OVERWRITE || mode > AK_STORE_FOLD || (mode == AK_STORE_INIT && !init))
         return AK_ERR_INVALID_ARG;
     if (src && !aligned(src, ak_dtype_size(in) >= 16 ? 16 : ak_dtype_size(in))) return AK_ERR_INVALID_ARG;
@@ -289,6 +296,8 @@ extern "C" ak_status ak_reduce(const void* src, int64_t n, ak_dtype in, ak_map f
 
     ReduceCall c;
     c.src = src;
+    c.src2 = src2;
+    c.map2 = map2;
     c.n = n;
     c.in = in;
     c.acc = acc;
@@ -325,6 +334,24 @@ extern "C" ak_status ak_reduce(const void* src, int64_t n, ak_dtype in, ak_map f
     return AK_OK;
 }
 
+extern "C" ak_status ak_reduce(const void* src, int64_t n, ak_dtype in, ak_map f, ak_op op, ak_dtype acc,
+                               ak_dtype out, const void* init, ak_store mode, void* dst_dev, void* dst_host,
+                               void* ws, size_t ws_bytes, const ak_opts* opts, void* stream) {
+    return reduce_impl(src, nullptr, 0, n, in, f, op, acc, out, init, mode, dst_dev, dst_host, ws, ws_bytes, opts,
+                       stream);
+}
+
+extern "C" ak_status ak_reduce2(const void* src_a, const void* src_b, int64_t n, ak_dtype in, ak_map2 f,
+                                ak_op op, ak_dtype acc, ak_dtype out, const void* init, ak_store mode,
+                                void* dst_dev, void* dst_host, void* ws, size_t ws_bytes, const ak_opts* opts,
+                                void* stream) {
+    if (n > 0 && !src_b) return AK_ERR_INVALID_ARG;
+    // a fused element needs a second source even when n == 0 decides nothing
+    const void* b = src_b ? src_b : reinterpret_cast<const void*>(uintptr_t(256));
+    return reduce_impl(src_a, b, (int)f, n, in, AK_MAP_IDENTITY, op, acc, out, init, mode, dst_dev, dst_host, ws,
+                       ws_bytes, opts, stream);
+}
+
 // ===========================================================================
 // ak_reduce_dims
 // ===========================================================================
@@ -332,28 +359,35 @@ extern "C" ak_status ak_reduce(const void* src, int64_t n, ak_dtype in, ak_map f
 namespace {
 
 // Merged view of a dims reduction: size-1 dimensions dropped, neighbouring
-// dimensions of the same kind (kept / reduced) merged.
+// dimensions of the same kind (kept / reduced) merged when the source
+// strides continue each other (always, for a dense array).
 struct Canon {
     int64_t nout, nfold;
     int nseg;
     int64_t ext[8];
+    int64_t st[8];  // source stride (elements) of each merged dimension
     bool red[8];
 };
 
-ak_status canonicalize(int ndim, const int64_t* shape, uint32_t mask, Canon* c) {
+ak_status canonicalize(int ndim, const int64_t* shape, const int64_t* strides, uint32_t mask, Canon* c) {
     if (ndim < 1 || ndim > 8 || !shape) return AK_ERR_INVALID_ARG;
     if (mask >> ndim) return AK_ERR_INVALID_ARG;
     c->nout = c->nfold = 1;
     c->nseg = 0;
+    int64_t dense = 1;
     for (int d = 0; d < ndim; ++d) {
-        if (shape[d] < 0) return AK_ERR_INVALID_ARG;
+        if (shape[d] < 0 || (strides && strides[d] < 0)) return AK_ERR_INVALID_ARG;
+        const int64_t sd = strides ? strides[d] : dense;
+        dense *= shape[d];
         const bool r = (mask >> d) & 1u;
         if (r) c->nfold *= shape[d];
         else c->nout *= shape[d];
         if (shape[d] == 1) continue;
-        if (c->nseg > 0 && c->red[c->nseg - 1] == r) c->ext[c->nseg - 1] *= shape[d];
+        const int q = c->nseg - 1;
+        if (q >= 0 && c->red[q] == r && sd == c->st[q] * c->ext[q]) c->ext[q] *= shape[d];
         else {
             c->ext[c->nseg] = shape[d];
+            c->st[c->nseg] = sd;
             c->red[c->nseg] = r;
             ++c->nseg;
         }
@@ -361,25 +395,38 @@ ak_status canonicalize(int ndim, const int64_t* shape, uint32_t mask, Canon* c) 
     return AK_OK;
 }
 
-// Fill the DimsCall's canonical fields; returns 0 strided/rows, 1 whole-array.
+// Fill the DimsCall's canonical fields; returns 0 strided / rows / general,
+// 1 whole-array (one output over one contiguous range).
 int classify(const Canon& cn, DimsCall* c) {
     c->general = false;
     c->inner = c->red = c->outer = 1;
+    c->ldj = c->ldk = 0;
     if (cn.nseg == 0) return 0;  // a single element
     if (cn.nseg == 1) {
-        if (cn.red[0]) return 1;  // one output over one contiguous range
-        c->inner = cn.ext[0];
-        return 0;
-    }
-    if (cn.nseg == 2) {
-        if (cn.red[0]) { c->red = cn.ext[0]; c->outer = cn.ext[1]; }
-        else { c->inner = cn.ext[0]; c->red = cn.ext[1]; }
-        return 0;
-    }
-    if (cn.nseg == 3 && !cn.red[0]) {
+        if (cn.red[0] && cn.st[0] == 1) return 1;
+        if (!cn.red[0] && cn.st[0] == 1) {
+            c->inner = cn.ext[0];
+            return 0;
+        }
+    } else if (cn.nseg == 2 && cn.red[0] != cn.red[1]) {
+        if (cn.red[0] && cn.st[0] == 1) {  // rows: contiguous reductions at stride ldk
+            c->red = cn.ext[0];
+            c->outer = cn.ext[1];
+            c->ldk = cn.st[1];
+            return 0;
+        }
+        if (!cn.red[0] && cn.st[0] == 1) {  // strided: contiguous outputs, rows at stride ldj
+            c->inner = cn.ext[0];
+            c->red = cn.ext[1];
+            c->ldj = cn.st[1];
+            return 0;
+        }
+    } else if (cn.nseg == 3 && !cn.red[0] && cn.red[1] && !cn.red[2] && cn.st[0] == 1) {
         c->inner = cn.ext[0];
         c->red = cn.ext[1];
         c->outer = cn.ext[2];
+        c->ldj = cn.st[1];
+        c->ldk = cn.st[2];
         return 0;
     }
     c->general = true;
@@ -395,9 +442,9 @@ struct DimsSetup {
     size_t ws_bytes;
 };
 
-ak_status setup_dims(const void* src, int ndim, const int64_t* shape, uint32_t mask, ak_dtype in, ak_dtype acc,
-                     const ak_opts& o, DimsSetup* d) {
-    ak_status s = canonicalize(ndim, shape, mask, &d->cn);
+ak_status setup_dims(const void* src, int ndim, const int64_t* shape, const int64_t* strides, uint32_t mask,
+                     ak_dtype in, ak_dtype acc, const ak_opts& o, DimsSetup* d) {
+    ak_status s = canonicalize(ndim, shape, strides, mask, &d->cn);
     if (s != AK_OK) return s;
     memset(&d->c, 0, sizeof d->c);
     d->c.src = src;
@@ -409,7 +456,12 @@ ak_status setup_dims(const void* src, int ndim, const int64_t* shape, uint32_t m
     d->c.auto_cluster = true;
     d->c.ndim = ndim;
     d->c.mask = mask;
-    for (int i = 0; i < ndim; ++i) d->c.shape[i] = shape[i];
+    int64_t dense = 1;
+    for (int i = 0; i < ndim; ++i) {
+        d->c.shape[i] = shape[i];
+        d->c.stride[i] = strides ? strides[i] : dense;
+        dense *= shape[i];
+    }
     d->path = classify(d->cn, &d->c);
     d->ws_bytes = kWsHeader;
     if (d->cn.nout == 0 || d->cn.nfold == 0) return AK_OK;
@@ -427,8 +479,9 @@ ak_status setup_dims(const void* src, int ndim, const int64_t* shape, uint32_t m
 
 }  // namespace
 
-extern "C" ak_status ak_reduce_dims_workspace_size(int ndim, const int64_t* shape, uint32_t dims_mask, ak_dtype in,
-                                                   ak_dtype acc, const ak_opts* opts, size_t* bytes) {
+extern "C" ak_status ak_reduce_dims_workspace_size(int ndim, const int64_t* shape, const int64_t* strides,
+                                                   uint32_t dims_mask, ak_dtype in, ak_dtype acc, const ak_opts* opts,
+                                                   size_t* bytes) {
     if (!bytes || !valid_dtype(in) || !valid_dtype(acc)) return AK_ERR_INVALID_ARG;
     if (opts && (opts->dims_shape < AK_SHAPE_AUTO || opts->dims_shape > AK_SHAPE_COLUMNS)) return AK_ERR_INVALID_ARG;
     const ak_opts o = resolve_opts(opts);
@@ -442,7 +495,8 @@ extern "C" ak_status ak_reduce_dims_workspace_size(int ndim, const int64_t* shap
         if (variant & 2) ov.flags &= ~AK_FLAG_DIMS_CLUSTER;
         DimsSetup d;
         const uintptr_t addr = 256 + ((variant & 1) ? ak_dtype_size(in) : 0);
-        ak_status s = setup_dims(reinterpret_cast<const void*>(addr), ndim, shape, dims_mask, in, acc, ov, &d);
+        ak_status s = setup_dims(reinterpret_cast<const void*>(addr), ndim, shape, strides, dims_mask, in, acc, ov,
+                                 &d);
         if (s != AK_OK) return s;
         if (variant & 2) {
             // the same call planned without the cluster combine
@@ -462,8 +516,8 @@ extern "C" ak_status ak_reduce_dims_workspace_size(int ndim, const int64_t* shap
     return AK_OK;
 }
 
-extern "C" ak_status ak_reduce_dims(const void* src, int ndim, const int64_t* shape, uint32_t dims_mask,
-                                    ak_dtype in, ak_map f, ak_op op, ak_dtype acc, ak_dtype out,
+extern "C" ak_status ak_reduce_dims(const void* src, int ndim, const int64_t* shape, const int64_t* strides,
+                                    uint32_t dims_mask, ak_dtype in, ak_map f, ak_op op, ak_dtype acc, ak_dtype out,
                                     const void* init, ak_store mode, void* dst, void* ws, size_t ws_bytes,
                                     const ak_opts* opts, void* stream) {
     ak_status s = check_types(in, f, op, acc, out);
@@ -473,7 +527,7 @@ extern "C" ak_status ak_reduce_dims(const void* src, int ndim, const int64_t* sh
     if (opts && (opts->dims_shape < AK_SHAPE_AUTO || opts->dims_shape > AK_SHAPE_COLUMNS)) return AK_ERR_INVALID_ARG;
     const ak_opts o = resolve_opts(opts);
     DimsSetup d;
-    s = setup_dims(src, ndim, shape, dims_mask, in, acc, o, &d);
+    s = setup_dims(src, ndim, shape, strides, dims_mask, in, acc, o, &d);
     if (s != AK_OK) return s;
     const int64_t nin = d.cn.nout * d.cn.nfold;
     if ((nin > 0 && !src) || (d.cn.nout > 0 && !dst)) return AK_ERR_INVALID_ARG;
@@ -497,6 +551,8 @@ extern "C" ak_status ak_reduce_dims(const void* src, int ndim, const int64_t* sh
     if (d.path == 1) {
         ReduceCall c;
         c.src = src;
+        c.src2 = nullptr;
+        c.map2 = 0;
         c.n = d.cn.nfold;
         c.in = in;
         c.acc = acc;
@@ -586,6 +642,7 @@ extern "C" ak_status ak_accumulate(const void* src, void* dst, int ndim, const i
     s = scan_geometry(ndim, shape, dim, &inner, &len, &outer);
     if (s != AK_OK) return s;
     const int64_t n = inner * len * outer;
+    if (opts && (opts->exclusive < 0 || opts->exclusive > 1 || opts->reserved != 0)) return AK_ERR_INVALID_ARG;
     if (n == 0) return AK_OK;
     if (!src || !dst) return AK_ERR_INVALID_ARG;
     const size_t isz = ak_dtype_size(in), osz = ak_dtype_size(out);
@@ -613,8 +670,15 @@ extern "C" ak_status ak_accumulate(const void* src, void* dst, int ndim, const i
     c.op = op;
     c.no_neutral = o.no_neutral != 0;
     c.has_init = init != nullptr;
+    c.exclusive = o.exclusive != 0;
     memset(c.init.b, 0, sizeof c.init.b);
     if (init) memcpy(c.init.b, init, ak_dtype_size(acc));
+    if (c.exclusive && !init) {
+        // the first output is the empty prefix: the neutral element stands
+        // for init where one exists (+0.0 for a float sum, as Julia's zero)
+        if (c.no_neutral || !neutral_value(op, acc, &c.init)) return AK_ERR_EMPTY_NO_INIT;
+        c.has_init = true;
+    }
     c.ws = ws;
     c.ws_bytes = ws_bytes;
     c.target_blocks = o.target_blocks;
@@ -631,4 +695,72 @@ extern "C" ak_status ak_accumulate(const void* src, void* dst, int ndim, const i
     cudaError_t e = cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e);
     return word == c.epoch ? AK_ERR_TIMEOUT : AK_OK;
+}
+
+extern "C" ak_status ak_scan_status(const void* ws) {
+    if (!ws || !aligned(ws, 16)) return AK_ERR_INVALID_ARG;
+    // the call clears the whole header before its kernel, and a kernel that
+    // gives up writes its (non-zero) epoch into the first word
+    uint64_t word = 0;
+    cudaError_t e = cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return word != 0 ? AK_ERR_TIMEOUT : AK_OK;
+}
+
+// ===========================================================================
+// ak_findall
+// ===========================================================================
+
+extern "C" ak_status ak_findall_workspace_size(int64_t n, ak_dtype in, const ak_opts* opts, size_t* bytes) {
+    (void)opts;
+    if (!bytes || n < 0 || !valid_dtype(in)) return AK_ERR_INVALID_ARG;
+    int64_t ntiles;
+    size_t ws, count_off;
+    ak_status s = plan_findall(n, in, &ntiles, &ws, &count_off);
+    if (s != AK_OK) return s;
+    *bytes = ws;
+    return AK_OK;
+}
+
+extern "C" ak_status ak_findall(const void* src, int64_t n, ak_dtype in, int64_t* idx, int64_t* count_dev,
+                                int64_t* count_host, void* ws, size_t ws_bytes, const ak_opts* opts,
+                                void* stream) {
+    if (!valid_dtype(in) || n < 0 || (!count_dev && !count_host)) return AK_ERR_INVALID_ARG;
+    int64_t ntiles;
+    size_t need, count_off;
+    ak_status s = plan_findall(n, in, &ntiles, &need, &count_off);
+    if (s != AK_OK) return s;
+    const size_t esz = ak_dtype_size(in);
+    if (n > 0 && (!src || !idx || !aligned(src, esz) || !aligned(idx, 8))) return AK_ERR_INVALID_ARG;
+    if (count_dev && !aligned(count_dev, 8)) return AK_ERR_INVALID_ARG;
+    const ak_opts o = resolve_opts(opts);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n == 0) {
+        if (count_host) *count_host = 0;
+        if (count_dev) {
+            Value16 zero;
+            memset(zero.b, 0, sizeof zero.b);
+            s = run_fill(count_dev, 1, AK_I64, zero, st);
+            if (s == AK_OK && o.check) s = sync_and_check(st);
+            return s;
+        }
+        return AK_OK;
+    }
+    if (!ws || ws_bytes < need || !aligned(ws, 16)) return AK_ERR_WORKSPACE;
+    int64_t* count = count_dev ? count_dev : reinterpret_cast<int64_t*>(static_cast<char*>(ws) + count_off);
+    const uint64_t epoch = next_epoch();
+    s = run_findall(src, n, in, idx, count, ws, ntiles, need, epoch, o.wait_limit_ns, o.debug_skip_publish_tile,
+                    o.target_blocks, st);
+    if (s != AK_OK) return s;
+    if (count_host) {
+        cudaError_t e = cudaMemcpyAsync(count_host, count, sizeof(int64_t), cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (!count_host && !o.check) return AK_OK;
+    s = sync_and_check(st);
+    if (s != AK_OK || !o.check) return s;
+    uint64_t word = 0;
+    cudaError_t e = cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return word == epoch ? AK_ERR_TIMEOUT : AK_OK;
 }

@@ -159,6 +159,74 @@ __global__ void __launch_bounds__(kBlockOrd) k_reduce_pass1_ordered(const In* __
     }
 }
 
+// First pass over a fused two-source element f(a_i, b_i) (commutative
+// operators). VB = 32: both sources share their offset within 32 bytes, so
+// the 32-byte vectors of a and b line up (block 0 adds the unaligned head, the
+// last block the tail, as in k_reduce_pass1); VB = sizeof(In): element-wise
+// loads, coalesced across the block, for sources of different alignments.
+template <class In, class Acc, class Out, class Map2, class M, int VB>
+__global__ void __launch_bounds__(kBlock) k_reduce2_pass1(const In* __restrict__ a, const In* __restrict__ b,
+                                                          int64_t n, int64_t head, int64_t nvec,
+                                                          typename M::P* __restrict__ partials,
+                                                          StoreSpec<Acc, Out, M> st) {
+    using P = typename M::P;
+    constexpr int V = VB / (int)sizeof(In);
+    __shared__ P smem[kBlock / kWarp];
+    auto elem = [](In u, In v) { return M::lift(Map2::apply(convert<Acc>(u), convert<Acc>(v))); };
+
+    P acc[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) acc[k] = M::empty();
+    const In* ba = a + head;
+    const In* bb = b + head;
+    const int64_t per = (nvec + gridDim.x - 1) / gridDim.x;
+    const int64_t vb = (int64_t)blockIdx.x * per;
+    const int64_t ve = min(nvec, vb + per);
+    int64_t v = vb + threadIdx.x;
+    for (; v + (kUnroll - 1) * kBlock < ve; v += kUnroll * kBlock) {
+        if constexpr (VB == 32) {
+            Raw<32> ra[kUnroll], rb[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                ra[u] = ld_stream32(ba + (v + u * kBlock) * V);
+                rb[u] = ld_stream32(bb + (v + u * kBlock) * V);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+                for (int k = 0; k < V; ++k)
+                    acc[k] = M::combine(acc[k], elem(raw_get<In>(ra[u], k), raw_get<In>(rb[u], k)));
+        } else {
+            In ra[kUnroll], rb[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                ra[u] = ba[v + u * kBlock];
+                rb[u] = bb[v + u * kBlock];
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) acc[0] = M::combine(acc[0], elem(ra[u], rb[u]));
+        }
+    }
+    for (; v < ve; v += kBlock) {
+#pragma unroll
+        for (int k = 0; k < V; ++k) acc[k] = M::combine(acc[k], elem(ba[v * V + k], bb[v * V + k]));
+    }
+    if (blockIdx.x == 0 && threadIdx.x < head) acc[0] = M::combine(acc[0], elem(a[threadIdx.x], b[threadIdx.x]));
+    const int64_t tail = head + nvec * V;
+    if (blockIdx.x == gridDim.x - 1 && tail + threadIdx.x < n)
+        acc[V - 1] = M::combine(acc[V - 1], elem(a[tail + threadIdx.x], b[tail + threadIdx.x]));
+
+    griddep_launch_dependents();
+    P r = acc[0];
+#pragma unroll
+    for (int k = 1; k < V; ++k) r = M::combine(r, acc[k]);
+    r = block_reduce<M, kBlock>(r, smem);
+    if (threadIdx.x == 0) {
+        if (gridDim.x == 1) store_result<Acc, Out, M>(r, st);
+        else partials[blockIdx.x] = r;
+    }
+}
+
 // Second pass: one block folds the partials in block order and stores.
 template <class Acc, class Out, class M>
 __global__ void __launch_bounds__(kFinishBlock) k_reduce_finish(const typename M::P* partials, int g,
@@ -216,6 +284,44 @@ ak_status launch(const ReduceCall& c, const ReducePlan& plan) {
     if (g > 1) {
         cudaError_t e = launch_pdl(k_reduce_finish<Acc, Out, M>, 1, kFinishBlock, c.stream,
                                    (const P*)partials, g, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        count_launches(1);
+    }
+    return AK_OK;
+}
+
+// The fused two-source reduction: first pass over f(a_i, b_i), then the
+// same one-block finish.
+template <class In, class Acc, class Out, class Map2, class M>
+ak_status launch2(const ReduceCall& c, const ReducePlan& plan) {
+    static_assert(M::commutative, "fused sources take commutative operators");
+    using P = typename M::P;
+    StoreSpec<Acc, Out, M> st;
+    st.mode = c.mode;
+    memcpy(&st.init, c.init.b, sizeof(Acc));
+    st.dst = static_cast<Out*>(c.dst);
+    st.bare = static_cast<P*>(c.bare);
+    P* partials = reinterpret_cast<P*>(static_cast<char*>(c.ws) + plan.partials_off);
+    const In* a = static_cast<const In*>(c.src);
+    const In* b = static_cast<const In*>(c.src2);
+    const int g = plan.grid;
+    const uintptr_t aa = reinterpret_cast<uintptr_t>(a), ab = reinterpret_cast<uintptr_t>(b);
+    if (aa % kVecBytes == ab % kVecBytes) {
+        constexpr int V = kVecBytes / sizeof(In);
+        int64_t head = (int64_t)(((kVecBytes - aa % kVecBytes) % kVecBytes) / sizeof(In));
+        head = std::min<int64_t>(head, c.n);
+        const int64_t nvec = (c.n - head) / V;
+        k_reduce2_pass1<In, Acc, Out, Map2, M, kVecBytes><<<g, kBlock, 0, c.stream>>>(a, b, c.n, head, nvec,
+                                                                                      partials, st);
+    } else {
+        k_reduce2_pass1<In, Acc, Out, Map2, M, (int)sizeof(In)><<<g, kBlock, 0, c.stream>>>(a, b, c.n, 0, c.n,
+                                                                                           partials, st);
+    }
+    ak_status s = check_launch();
+    if (s != AK_OK) return s;
+    count_launches(1);
+    if (g > 1) {
+        cudaError_t e = launch_pdl(k_reduce_finish<Acc, Out, M>, 1, kFinishBlock, c.stream, (const P*)partials, g, st);
         if (e != cudaSuccess) return cuda_fail(e);
         count_launches(1);
     }

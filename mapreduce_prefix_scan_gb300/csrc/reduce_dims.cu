@@ -76,11 +76,18 @@ static void select_shape(int64_t I, int64_t J, int64_t K, int esz, int vec, int 
     if (shape == AK_SHAPE_COLUMNS && cluster_ok) {
         // Prefer a cluster split (2..16 blocks per output tile, partials
         // combined in distributed shared memory): try row segments of 32,
-        // 16, 8 and 4 threads until the wanted split fits a cluster.
+        // 16, 8 and 4 threads until the wanted split fits a cluster. These
+        // inputs are latency-bound: aim at about 16 KB a block (4 rows of
+        // 16-byte loads in flight per thread), the size at which a plain
+        // read of a 12.6 MB array was fastest on GB300.
+        const int64_t per_block_c = (int64_t)kBlock * 4 * 16;
+        const int64_t target_c = std::max<int64_t>(sm_count, std::min<int64_t>((int64_t)sm_count * 8,
+                                                                               (bytes + per_block_c - 1) / per_block_c));
         for (int tpr : {32, 16, 8, 4}) {
             if (tpr > vecs_per_row && tpr != 4) continue;
             const int64_t tiles = set_tile((int)std::min<int64_t>(tpr, vecs_per_row));
-            const int64_t want = (target + tiles - 1) / tiles;
+            if (kBlock % p->tile_out != 0) continue;
+            const int64_t want = (target_c + tiles - 1) / tiles;
             if (want <= 1) {
                 p->split = 1;
                 p->shape = AK_SHAPE_TILED;
@@ -121,7 +128,25 @@ ak_status plan_dims(const DimsCall& c, const DeviceInfo& dev, DimsPlan* p) {
     p->tile_out = 1;
     p->row_groups = 1;
     p->shape = AK_SHAPE_THREAD;
-    if (c.general) return AK_OK;
+    if (c.general) {
+        // many outputs: a thread per output; few: blocks of (output, split)
+        // pairs, split until the device has a few blocks per SM
+        int64_t nout = 1, nfold = 1;
+        for (int d = 0; d < c.ndim; ++d) {
+            if ((c.mask >> d) & 1u) nfold *= c.shape[d];
+            else nout *= c.shape[d];
+        }
+        if (nout >= (int64_t)dev.sm_count * kBlock * 4 || nout > 65535 * 1024) return AK_OK;
+        p->shape = AK_SHAPE_TILED;
+        int64_t split = ((int64_t)dev.sm_count * 4 + nout - 1) / nout;
+        split = std::max<int64_t>(1, std::min<int64_t>({split, (nfold + 4095) / 4096, 65535}));
+        p->split = (int)split;
+        if (split > 1) {
+            p->shape = AK_SHAPE_COLUMNS;
+            p->ws_bytes = align_up(kWsHeader + (size_t)split * nout * psz, 256);
+        }
+        return AK_OK;
+    }
     if (c.inner == 1) {
         // contiguous reduction: split long rows when there are few outputs
         const int64_t target_warps = (int64_t)dev.sm_count * 64;
@@ -132,7 +157,9 @@ ak_status plan_dims(const DimsCall& c, const DeviceInfo& dev, DimsPlan* p) {
     } else {
         const uintptr_t addr = reinterpret_cast<uintptr_t>(c.src);
         int vec = 1;
-        if (esz < 16 && addr % 16 == 0 && (c.inner * (int64_t)esz) % 16 == 0) vec = (int)(16 / esz);
+        if (esz < 16 && addr % 16 == 0 && (c.inner * (int64_t)esz) % 16 == 0 && (c.ldj * (int64_t)esz) % 16 == 0 &&
+            (c.outer == 1 || (c.ldk * (int64_t)esz) % 16 == 0))
+            vec = (int)(16 / esz);
         select_shape(c.inner, c.red, c.outer, (int)esz, vec, dev.sm_count, c.forced_shape, c.allow_cluster,
                      c.auto_cluster, p);
     }

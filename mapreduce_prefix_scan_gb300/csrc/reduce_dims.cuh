@@ -1,32 +1,39 @@
-// reduce_dims.cuh -- kernels of the reductions over a set of dimensions of a dense
-// column-major array on GB300.
+// reduce_dims.cuh -- kernels of the reductions over a set of dimensions of a
+// column-major array (dense, or a strided view) on GB300.
 //
 // After merging dimensions (api.cu), most problems take one of two canonical
-// forms:
-//   strided  out[i + I*k] = fold_j x[i + I*(j + J*k)]   (I > 1: outputs are
-//            contiguous, the reduction walks rows at stride I: sum(x; dims=2)
-//            of a matrix, the middle dimension of a 3-d array)
-//   rows     out[k]       = fold_j x[j + J*k]           (contiguous reduction)
-// anything else goes to a general one-thread-per-output kernel.
+// forms (ldj, ldk: source strides in elements; a dense array has ldj = I,
+// ldk = I*J):
+//   strided  out[i + I*k] = fold_j x[i + ldj*j + ldk*k]   (I > 1: outputs are
+//            contiguous in the source, the reduction walks rows: sum(x;
+//            dims=2) of a matrix, the middle dimension of a 3-d array)
+//   rows     out[k]       = fold_j x[j + ldk*k]           (contiguous reduction)
+// anything else (a kept dimension without unit stride, several reduced
+// blocks that do not merge) goes to a general kernel.
 //
-// Strided kernel (strided-reduction PR #176, item 1 and the paragraph after
-// it: a fixed 2-d block of outputs x reduction rows, split across blocks only
-// when the outputs alone do not fill the device; item 2: runs of contiguous
-// outputs at the offsets of the other kept dimensions, so the middle
-// dimension of a 3-d array takes the same kernel). A block owns a tile of
-// `tile_out` consecutive outputs of one run k and a range of reduction rows.
-// Its threads form `row_groups` groups of `tpr` threads; a group covers the
-// tile's row segment with 16-byte vector loads and walks a contiguous
-// sub-range of rows with several rows in flight. Groups are combined in row
-// order through shared memory, so non-commutative operators keep their
-// order. With a split, per-split partials go to the workspace and a second
-// pass (programmatic dependent launch) folds them in split order.
+// Strided kernel (strided-reduction PR #176, "This PR" item 1 and the
+// paragraph after it: a fixed 2-d block of outputs by reduction rows, split
+// across blocks only when the outputs alone cannot fill the device; item 2:
+// a 3-d reduction over the middle dimension becomes one run of contiguous
+// outputs per outer index k, handled by the same kernel). A block owns a
+// tile of `tile_out` consecutive outputs of one run k and a range of
+// reduction rows. Its threads form `row_groups` groups of `tpr` threads; a
+// group covers the tile's row segment with 16-byte vector loads and walks a
+// contiguous sub-range of rows with all of its rows' loads in flight. Groups
+// are combined in row order (a few threads per output and an ordered shuffle
+// tree), so non-commutative operators keep their order. The reduction is
+// split across blocks when the outputs alone do not fill the device: the
+// blocks of one output tile either form a thread-block cluster and push
+// their partials into the owning block's shared memory (small inputs: one
+// launch, one cluster barrier), or write per-split partials that a second
+// pass (programmatic dependent launch) folds in split order.
 //
 // The three shapes of the pages are parameter regimes of this one kernel:
 // "thread" = one group (each thread owns vec outputs and walks all rows),
 // "tiled" = several groups, no split, "columns" = several groups and a split.
 #pragma once
 #include <algorithm>
+#include <atomic>
 #include <cooperative_groups.h>
 
 #include "ak_common.cuh"
@@ -36,7 +43,8 @@ namespace ak {
 namespace dims {
 
 constexpr int kBlock = 256;
-constexpr int kUnroll = 8;          // rows in flight per thread
+constexpr int kUnroll = 8;          // rows in flight per thread (at most)
+constexpr int kMaxClusterSplit = 16;  // blocks of an output tile combined in one cluster
 constexpr int kMinRowsPerGroup = 8; // the selector splits no further than this many rows per group
 
 template <class Acc, class Out, class M>
@@ -61,17 +69,19 @@ __device__ __forceinline__ typename M::P lift_elem(In x) {
     return M::lift(Map::apply(convert<Acc>(x)));
 }
 
-// One row segment of VB bytes: a 16-byte streaming vector load, or a single
-// element.
+// One row segment of VB bytes, kept as raw words until its elements are
+// used (8 bf16 stay in 4 registers): a 16-byte streaming vector load, or a
+// single element.
 template <class In, int VB>
-__device__ __forceinline__ void load_row(const In* p, In (&r)[VB / sizeof(In)]) {
-    if constexpr (VB == 16 && sizeof(In) < 16) {
-        Raw<16> t = ld_stream16(p);
-        memcpy(r, &t, 16);
-    } else {
-        r[0] = *p;
+struct RowSeg {
+    static constexpr bool kVec = VB == 16 && sizeof(In) < 16;
+    Raw<kVec ? 16 : (sizeof(In) < 4 ? 4 : (int)sizeof(In))> raw;
+    __device__ __forceinline__ void load(const In* p) {
+        if constexpr (kVec) raw = ld_stream16(p);
+        else memcpy(&raw, p, sizeof(In));
     }
-}
+    __device__ __forceinline__ In get(int q) const { return raw_get<In>(raw, q); }
+};
 
 // VB = bytes per load: 16 (vector of 16/sizeof(In) outputs) or sizeof(In).
 // CLUSTER: the `split` blocks of one output tile form a thread-block
@@ -82,8 +92,9 @@ __device__ __forceinline__ void load_row(const In* p, In (&r)[VB / sizeof(In)]) 
 // pass. Otherwise blockIdx.y is the split index and split > 1 writes
 // partials for k_dims_finish.
 template <class In, class Acc, class Out, class Map, class M, int VB, bool CLUSTER>
-__global__ void __launch_bounds__(kBlock) k_dims_strided(const In* __restrict__ x, int64_t I, int64_t J,
-                                                         int64_t K, int tile_out, int tpr, int R,
+__global__ void __launch_bounds__(kBlock, CLUSTER ? 6 : 4) k_dims_strided(const In* __restrict__ x, int64_t I, int64_t J,
+                                                         int64_t K, int64_t ldj, int64_t ldk, int tile_out, int tpr,
+                                                         int R,
                                                          int split, typename M::P* __restrict__ partials,
                                                          DimsStore<Acc, Out, M> st) {
     using P = typename M::P;
@@ -107,31 +118,41 @@ __global__ void __launch_bounds__(kBlock) k_dims_strided(const In* __restrict__ 
     for (int q = 0; q < V; ++q) acc[q] = M::empty();
 
     if (rg < R && i0 < I) {
-        const In* base = x + i0 + I * J * k;
+        const In* base = x + i0 + ldk * k;
         if (i0 + V <= I) {
+            // ROWS rows per round, all loads issued before any is used; a
+            // short last round is predicated, not walked row by row. The
+            // cluster plans (small inputs) give each group about 4 rows.
+            constexpr int ROWS = CLUSTER ? 4 : kUnroll;
             int64_t j = jr;
-            for (; j + kUnroll <= jre; j += kUnroll) {
-                In r[kUnroll][V];
+            for (; j + ROWS <= jre; j += ROWS) {
+                RowSeg<In, VB> r[ROWS];
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) load_row<In, VB>(base + I * (j + u), r[u]);
+                for (int u = 0; u < ROWS; ++u) r[u].load(base + ldj * (j + u));
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u)
+                for (int u = 0; u < ROWS; ++u)
 #pragma unroll
                     for (int q = 0; q < V; ++q)
-                        acc[q] = M::combine(acc[q], lift_elem<In, Acc, Map, M>(r[u][q]));
+                        acc[q] = M::combine(acc[q], lift_elem<In, Acc, Map, M>(r[u].get(q)));
             }
-            for (; j < jre; ++j) {
-                In r[V];
-                load_row<In, VB>(base + I * j, r);
+            if (j < jre) {
+                RowSeg<In, VB> r[ROWS];
 #pragma unroll
-                for (int q = 0; q < V; ++q) acc[q] = M::combine(acc[q], lift_elem<In, Acc, Map, M>(r[q]));
+                for (int u = 0; u < ROWS; ++u)
+                    if (j + u < jre) r[u].load(base + ldj * (j + u));
+#pragma unroll
+                for (int u = 0; u < ROWS; ++u)
+                    if (j + u < jre)
+#pragma unroll
+                        for (int q = 0; q < V; ++q)
+                            acc[q] = M::combine(acc[q], lift_elem<In, Acc, Map, M>(r[u].get(q)));
             }
         } else {
             // ragged last vector of the row: scalar loads of the valid columns
             for (int64_t j = jr; j < jre; ++j)
 #pragma unroll
                 for (int q = 0; q < V; ++q)
-                    if (i0 + q < I) acc[q] = M::combine(acc[q], lift_elem<In, Acc, Map, M>(base[I * j + q]));
+                    if (i0 + q < I) acc[q] = M::combine(acc[q], lift_elem<In, Acc, Map, M>(base[ldj * j + q]));
         }
     }
     griddep_launch_dependents();
@@ -142,39 +163,63 @@ __global__ void __launch_bounds__(kBlock) k_dims_strided(const In* __restrict__ 
         for (int q = 0; q < V; ++q) smem[rg * tile_out + c * V + q] = acc[q];
     }
     __syncthreads();
-    if constexpr (CLUSTER) {
-        // this block's partial outputs go to the front of smem (row groups
-        // combined in order), then the cluster folds them rank by rank
-        namespace cg = cooperative_groups;
-        cg::cluster_group cluster = cg::this_cluster();
-        P part[(kBlock * V + kBlock - 1) / kBlock];
-        int np = 0;
-        for (int o = tid; o < tile_out; o += kBlock, ++np) {
-            P a = smem[o];
-            for (int g = 1; g < R; ++g) a = M::combine(a, smem[g * tile_out + o]);
-            part[np] = a;
-        }
-        __syncthreads();
-        np = 0;
-        for (int o = tid; o < tile_out; o += kBlock, ++np) smem[o] = part[np];
-        cluster.sync();
-        const int per = (tile_out + split - 1) / split;
-        const int o = s * per + tid;
-        if (tid < per && o < tile_out) {
-            const int64_t i = ct * tile_out + o;
-            if (i < I) {
-                P a = *cluster.map_shared_rank(smem + o, 0);
-                for (int q = 1; q < split; ++q) a = M::combine(a, *cluster.map_shared_rank(smem + o, q));
-                dims_store<Acc, Out, M>(a, st, i + I * k);
-            }
-        }
-        cluster.sync();  // no block leaves while others read its shared memory
-    } else {
+    if (kBlock % tile_out != 0) {
+        // wide tiles (one row group; a tile of more than kBlock outputs or of
+        // a width that does not divide the block): a thread per output
         for (int o = tid; o < tile_out; o += kBlock) {
             const int64_t i = ct * tile_out + o;
             if (i >= I) continue;
             P a = smem[o];
             for (int g = 1; g < R; ++g) a = M::combine(a, smem[g * tile_out + o]);
+            if (split == 1) dims_store<Acc, Out, M>(a, st, i + I * k);
+            else if constexpr (!CLUSTER) partials[((int64_t)s * K + k) * I + i] = a;
+        }
+        return;
+    }
+    // The R row groups of output e are folded by G consecutive threads (each
+    // folds `per_t` consecutive groups, then an ordered shuffle tree within
+    // the G lanes): a short dependency chain instead of R serial combines.
+    // tile_out divides kBlock here, so G = kBlock / tile_out = R / V is a
+    // power of two (capped at a warp and at the number of row groups).
+    const int G0 = kBlock / tile_out;
+    const int G = min(min(G0, kWarp), R);  // powers of two; the thread shape has R = 1
+    const int per_t = R / G;
+    const int e = tid / G, h = tid % G;
+    P a = M::empty();
+    if (e < tile_out) {
+        a = smem[(h * per_t) * tile_out + e];
+        for (int g = 1; g < per_t; ++g) a = M::combine(a, smem[(h * per_t + g) * tile_out + e]);
+    }
+    for (int d = 1; d < G; d <<= 1) {
+        const P o = shfl_down_width(a, d, G);
+        if (h + d < G) a = M::combine(a, o);
+    }
+    // lane h == 0 of each group now holds output e's partial of this block
+    if constexpr (CLUSTER) {
+        // push: the owner rank of output e folds it; every block stores its
+        // partial straight into the owner's inbox (distributed shared
+        // memory), then one cluster barrier (release / acquire) makes the
+        // stores visible. Nothing reads another block's shared memory after
+        // the barrier, so blocks may leave as soon as they are done.
+        namespace cg = cooperative_groups;
+        cg::cluster_group cluster = cg::this_cluster();
+        __shared__ P inbox[kBlock + kMaxClusterSplit];
+        const int per = (tile_out + split - 1) / split;
+        if (h == 0 && e < tile_out) {
+            P* box = cluster.map_shared_rank(inbox, e / per);
+            box[s * per + e % per] = a;
+        }
+        cluster.sync();
+        const int eo = s * per + tid;
+        if (tid < per && eo < tile_out && ct * tile_out + eo < I) {
+            P r = inbox[tid];
+#pragma unroll 4
+            for (int q = 1; q < split; ++q) r = M::combine(r, inbox[q * per + tid]);
+            dims_store<Acc, Out, M>(r, st, ct * tile_out + eo + I * k);
+        }
+    } else {
+        const int64_t i = ct * tile_out + e;
+        if (h == 0 && e < tile_out && i < I) {
             if (split == 1) dims_store<Acc, Out, M>(a, st, i + I * k);
             else partials[((int64_t)s * K + k) * I + i] = a;
         }
@@ -183,7 +228,7 @@ __global__ void __launch_bounds__(kBlock) k_dims_strided(const In* __restrict__ 
 
 // Contiguous reduction: one warp per (output k, split s) segment.
 template <class In, class Acc, class Out, class Map, class M>
-__global__ void __launch_bounds__(kBlock) k_dims_rows(const In* __restrict__ x, int64_t J, int64_t K,
+__global__ void __launch_bounds__(kBlock) k_dims_rows(const In* __restrict__ x, int64_t J, int64_t K, int64_t ldk,
                                                       int split, typename M::P* __restrict__ partials,
                                                       DimsStore<Acc, Out, M> st) {
     using P = typename M::P;
@@ -195,7 +240,7 @@ __global__ void __launch_bounds__(kBlock) k_dims_rows(const In* __restrict__ x, 
     const int s = (int)(gw - k * split);
     const int64_t jper = div_fast(J + split - 1, split);
     const int64_t js = (int64_t)s * jper, je = min(J, js + jper);
-    const In* row = x + J * k;
+    const In* row = x + ldk * k;
     P a = M::empty();
     if constexpr (M::commutative) {
         int64_t j = js + lane;
@@ -246,8 +291,10 @@ __global__ void __launch_bounds__(kBlock) k_dims_finish(const typename M::P* par
     dims_store<Acc, Out, M>(a, st, o);
 }
 
-// General fallback for any dims mask: one thread per output, reduced indices
-// visited in increasing column-major order.
+// General fallback for any dims mask and any strides: reduced indices
+// visited in increasing column-major order. Many outputs: one thread per
+// output (k_dims_general); few outputs: blocks of (output, split) pairs
+// (k_dims_general_blocks).
 struct GeneralIndex {
     int ndim;
     int64_t shape[8];
@@ -281,6 +328,59 @@ __global__ void __launch_bounds__(kBlock) k_dims_general(const In* __restrict__ 
     dims_store<Acc, Out, M>(acc, st, o);
 }
 
+// Block (o, s) folds part s of output o's reduction: its threads take
+// consecutive ranges of the reduced index (walked with an odometer over the
+// reduced dimensions, one division per thread at the start), and the block
+// combines them in thread order, so every operator keeps its order. With
+// split > 1 partials[s * nout + o] go to k_dims_finish.
+template <class In, class Acc, class Out, class Map, class M>
+__global__ void __launch_bounds__(kBlock) k_dims_general_blocks(const In* __restrict__ x, GeneralIndex g, int split,
+                                                                typename M::P* __restrict__ partials,
+                                                                DimsStore<Acc, Out, M> st) {
+    using P = typename M::P;
+    __shared__ P smem[kBlock / kWarp];
+    const int64_t o = blockIdx.x;
+    const int s = (int)blockIdx.y;
+    int64_t base = 0, t = o;
+    for (int a = 0; a < g.nk; ++a) {
+        const int d = g.kept[a];
+        base += (t % g.shape[d]) * g.stride[d];
+        t /= g.shape[d];
+    }
+    const int64_t per = (g.nfold + split - 1) / split;
+    const int64_t rb = (int64_t)s * per, re = min(g.nfold, rb + per);
+    const int64_t tper = (max(re - rb, (int64_t)0) + kBlock - 1) / kBlock;
+    const int64_t r0 = rb + (int64_t)threadIdx.x * tper, r1 = min(re, r0 + tper);
+    P acc = M::empty();
+    if (r0 < r1) {
+        int64_t idx[8];
+        int64_t off = base, u = r0;
+        for (int a = 0; a < g.nr; ++a) {
+            const int d = g.red[a];
+            idx[a] = u % g.shape[d];
+            u /= g.shape[d];
+            off += idx[a] * g.stride[d];
+        }
+        for (int64_t r = r0; r < r1; ++r) {
+            acc = M::combine(acc, lift_elem<In, Acc, Map, M>(x[off]));
+            // next reduced index: odometer over the reduced dimensions
+            for (int a = 0; a < g.nr; ++a) {
+                const int d = g.red[a];
+                off += g.stride[d];
+                if (++idx[a] < g.shape[d]) break;
+                off -= g.shape[d] * g.stride[d];
+                idx[a] = 0;
+            }
+        }
+    }
+    griddep_launch_dependents();
+    acc = block_reduce<M, kBlock>(acc, smem);
+    if (threadIdx.x == 0) {
+        if (split == 1) dims_store<Acc, Out, M>(acc, st, o);
+        else partials[(int64_t)s * g.nout + o] = acc;
+    }
+}
+
 template <class Acc, class Out, class M, class... Args>
 cudaError_t launch_finish(dim3 grid, cudaStream_t s, Args... args) {
     cudaLaunchConfig_t cfg = {};
@@ -295,9 +395,30 @@ cudaError_t launch_finish(dim3 grid, cudaStream_t s, Args... args) {
     return cudaLaunchKernelEx(&cfg, k_dims_finish<Acc, Out, M>, args...);
 }
 
+// Whether clusters of `split` blocks of this kernel can be scheduled on the
+// current device at all (an MPS or green-context SM limit may forbid them),
+// cached per device and cluster size.
+template <class K>
+bool cluster_fits(K kernel, const cudaLaunchConfig_t& cfg, int split) {
+    static std::atomic<signed char> cache[64][kMaxClusterSplit + 1];  // 0 unknown, 1 fits, -1 does not
+    DeviceInfo dev;
+    if (!current_device(&dev) || dev.device >= 64 || split > kMaxClusterSplit) return false;
+    std::atomic<signed char>& slot = cache[dev.device][split];
+    const signed char known = slot.load(std::memory_order_relaxed);
+    if (known != 0) return known > 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    slot.store(n > 0 ? 1 : -1, std::memory_order_relaxed);
+    return n > 0;
+}
+
 template <class In, class Acc, class Out, class Map, class M>
-ak_status launch(const DimsCall& c, const DimsPlan& p) {
+ak_status launch(const DimsCall& c, const DimsPlan& plan) {
     using P = typename M::P;
+    DimsPlan p = plan;
     DimsStore<Acc, Out, M> st;
     st.mode = c.mode;
     memcpy(&st.init, c.init.b, sizeof(Acc));
@@ -307,33 +428,46 @@ ak_status launch(const DimsCall& c, const DimsPlan& p) {
     if (c.general) {
         GeneralIndex g = {};
         g.ndim = c.ndim;
-        int64_t stv = 1;
         g.nout = g.nfold = 1;
         for (int d = 0; d < c.ndim; ++d) {
             g.shape[d] = c.shape[d];
-            g.stride[d] = stv;
-            stv *= c.shape[d];
+            g.stride[d] = c.stride[d];
             if ((c.mask >> d) & 1u) { g.red[g.nr++] = d; g.nfold *= c.shape[d]; }
             else { g.kept[g.nk++] = d; g.nout *= c.shape[d]; }
         }
-        const int64_t blocks = (g.nout + kBlock - 1) / kBlock;
-        k_dims_general<In, Acc, Out, Map, M><<<(unsigned)blocks, kBlock, 0, c.stream>>>(x, g, st);
+        if (p.shape == AK_SHAPE_THREAD) {
+            const int64_t blocks = (g.nout + kBlock - 1) / kBlock;
+            k_dims_general<In, Acc, Out, Map, M><<<(unsigned)blocks, kBlock, 0, c.stream>>>(x, g, st);
+        } else {
+            k_dims_general_blocks<In, Acc, Out, Map, M><<<dim3((unsigned)g.nout, (unsigned)p.split), kBlock, 0,
+                                                         c.stream>>>(x, g, p.split, partials, st);
+        }
         ak_status s = check_launch();
-        if (s == AK_OK) count_launches(1);
-        return s;
+        if (s != AK_OK) return s;
+        count_launches(1);
+        if (p.split > 1) {
+            cudaError_t e = launch_finish<Acc, Out, M>(dim3((unsigned)((g.nout + kBlock - 1) / kBlock)), c.stream,
+                                                       (const P*)partials, g.nout, p.split, st);
+            if (e != cudaSuccess) return cuda_fail(e);
+            count_launches(1);
+        }
+        return AK_OK;
     }
     const int64_t nout = c.inner * c.outer;
     if (c.inner == 1) {
         const int64_t warps = c.outer * p.split;
         const int64_t blocks = (warps + kBlock / kWarp - 1) / (kBlock / kWarp);
-        k_dims_rows<In, Acc, Out, Map, M><<<(unsigned)blocks, kBlock, 0, c.stream>>>(x, c.red, c.outer, p.split,
-                                                                                    partials, st);
+        k_dims_rows<In, Acc, Out, Map, M><<<(unsigned)blocks, kBlock, 0, c.stream>>>(x, c.red, c.outer, c.ldk,
+                                                                                    p.split, partials, st);
     } else {
         const int64_t tiles_i = (c.inner + p.tile_out - 1) / p.tile_out;
         const int tpr = p.tile_out / p.vec;
         auto go = [&](auto vb) -> cudaError_t {
             constexpr int VB = decltype(vb)::value;
             if (p.cluster) {
+                // the cluster combine needs tiles that divide the block and at
+                // most kMaxClusterSplit blocks per tile (the selector's plans)
+                if (kBlock % p.tile_out != 0 || p.split > kMaxClusterSplit) return cudaErrorInvalidConfiguration;
                 auto kernel = k_dims_strided<In, Acc, Out, Map, M, VB, true>;
                 if (p.split > 8) {
                     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -350,12 +484,30 @@ ak_status launch(const DimsCall& c, const DimsPlan& p) {
                 attr[0].val.clusterDim.z = 1;
                 cfg.attrs = attr;
                 cfg.numAttrs = 1;
-                return cudaLaunchKernelEx(&cfg, kernel, x, c.inner, c.red, c.outer, p.tile_out, tpr, p.row_groups,
-                                          p.split, partials, st);
+                if (cluster_fits(kernel, cfg, p.split)) {
+                    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, x, c.inner, c.red, c.outer, c.ldj, c.ldk,
+                                                             p.tile_out, tpr, p.row_groups, p.split, partials, st);
+                    if (e != cudaErrorInvalidClusterSize && e != cudaErrorLaunchOutOfResources) return e;
+                    cudaGetLastError();
+                }
+                // no cluster of this size can run here: plan the same call
+                // with the workspace split and a second pass instead
+                DimsCall c2 = c;
+                c2.allow_cluster = c2.auto_cluster = false;
+                DeviceInfo dev;
+                if (!current_device(&dev)) return cudaErrorNoDevice;
+                if (plan_dims(c2, dev, &p) != AK_OK || p.cluster) return cudaErrorInvalidConfiguration;
+                if (c.ws_bytes < p.ws_bytes) return cudaErrorMemoryAllocation;
+                const int64_t tiles2 = (c.inner + p.tile_out - 1) / p.tile_out;
+                dim3 grid((unsigned)(tiles2 * c.outer), (unsigned)p.split);
+                k_dims_strided<In, Acc, Out, Map, M, VB, false><<<grid, kBlock, 0, c.stream>>>(
+                    x, c.inner, c.red, c.outer, c.ldj, c.ldk, p.tile_out, p.tile_out / p.vec, p.row_groups, p.split,
+                    partials, st);
+                return cudaGetLastError();
             }
             dim3 grid((unsigned)(tiles_i * c.outer), (unsigned)p.split);
             k_dims_strided<In, Acc, Out, Map, M, VB, false><<<grid, kBlock, 0, c.stream>>>(
-                x, c.inner, c.red, c.outer, p.tile_out, tpr, p.row_groups, p.split, partials, st);
+                x, c.inner, c.red, c.outer, c.ldj, c.ldk, p.tile_out, tpr, p.row_groups, p.split, partials, st);
             return cudaGetLastError();
         };
         cudaError_t e = cudaSuccess;
@@ -364,6 +516,7 @@ ak_status launch(const DimsCall& c, const DimsPlan& p) {
         } else {
             e = go(std::integral_constant<int, (int)sizeof(In)>{});
         }
+        if (e == cudaErrorMemoryAllocation) return AK_ERR_WORKSPACE;  // the fallback plan needs a larger workspace
         if (e != cudaSuccess) return cuda_fail(e);
     }
     ak_status s = check_launch();

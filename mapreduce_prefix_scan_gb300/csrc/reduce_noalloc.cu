@@ -13,6 +13,8 @@
 // AK_NOALLOC_SCRATCH_BYTES of it until the process exits.
 #include <mutex>
 
+#include <cuda.h>
+
 #include "ak_internal.h"
 
 // The scratch itself. In host code this name is only a host-side stand-in,
@@ -23,23 +25,62 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-// Device address of g_noalloc_scratch per device, looked up once per device
-// with that device current (the lookup is what the first call does).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The unique ID of the context current on this thread (driver calls reached
+// through the runtime's entry-point query, so nothing links libcuda); false
+// when no context is current yet or the driver lacks the query.
+bool current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        else
+            cudaGetLastError();
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+        else
+            cudaGetLastError();
+    });
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_noalloc_scratch for the current device, looked up with
+// that device current the first time and again whenever the device's context
+// has changed since (a cudaDeviceReset gives the device a new context, in
+// which the library's module, and so the array, sits at a new address).
 ak_status scratch_address(void** out) {
     static std::mutex mu;
     static void* addr[kMaxDevices] = {};
+    static unsigned long long ctx_of[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return ak::cuda_fail(e);
     if (dev < 0 || dev >= kMaxDevices) return AK_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p) return ak::cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
-        addr[dev] = p;
+    unsigned long long id = 0;
+    if (addr[dev] && current_context_id(&id) && id == ctx_of[dev]) {
+        *out = addr[dev];
+        return AK_OK;
     }
-    *out = addr[dev];
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return ak::cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+    // the lookup made the device's primary context current if it was not
+    if (!current_context_id(&id)) id = 0;  // unknown: looked up again on every call
+    addr[dev] = id != 0 ? p : nullptr;
+    ctx_of[dev] = id;
+    *out = p;
     return AK_OK;
 }
 

@@ -16,6 +16,10 @@
 //    one block per line, no state shared between blocks.
 //  * k_scan_strided -- lines along a strided dimension: a thread per column.
 //
+// Every kernel also writes the exclusive scan on request: element i then
+// holds the fold of init and the elements before it (the store takes the
+// running value before the element is combined instead of after).
+//
 // Tile scan (AcceleratedKernels.jl tile-scan PR #202, first two
 // paragraphs): a tile is loaded, each thread scans its own run of
 // consecutive elements, the run totals are scanned across the block, and
@@ -448,7 +452,7 @@ __device__ __forceinline__ void load_tile(char* tile, const In* src, int cnt, ui
 // then becomes the inclusive prefix of the tile (the next tile's carry).
 template <class Acc, class Out, class M, int ITEMS, int BLOCK>
 __device__ __forceinline__ void scan_apply_store(char* tile, Out* dst, int cnt, typename M::P* prefix,
-                                                 typename M::P* warp_tot, uint64_t policy) {
+                                                 typename M::P* warp_tot, uint64_t policy, bool excl) {
     using P = typename M::P;
     using L = RunLayout<Acc, ITEMS>;
     constexpr int W = BLOCK / kWarp;
@@ -489,10 +493,22 @@ __device__ __forceinline__ void scan_apply_store(char* tile, Out* dst, int cnt, 
         block_total = shfl_idx_any(wi, W - 1);
     }
     __syncthreads();
-    // apply the prefixes to the run, write back
+    // apply the prefixes to the run, write back (exclusive: element i takes
+    // the inclusive value of element i - 1, the first one the run's prefix,
+    // which is present: an exclusive scan always starts from init)
     const P base = M::combine(warp_tot[warp], lane_excl);
+    if (excl) {
+        Acc prev = M::value(base);
 #pragma unroll
-    for (int i = 0; i < ITEMS; ++i) run[i] = M::value(M::combine(base, M::lift(run[i])));
+        for (int i = 0; i < ITEMS; ++i) {
+            const Acc cur = M::value(M::combine(base, M::lift(run[i])));
+            run[i] = prev;
+            prev = cur;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < ITEMS; ++i) run[i] = M::value(M::combine(base, M::lift(run[i])));
+    }
     smem_store(L::run_ptr(tile, tid), run);
     __syncthreads();
     // striped (coalesced) store
@@ -666,7 +682,7 @@ __device__ __forceinline__ void store_chunk(Out* dst, const Out (&o)[CH], uint64
 // stored to dst.
 template <class In, class Out, class M, int SEG>
 __device__ __forceinline__ void segment_scan_store(const In* src, Out* dst, int n, typename M::P acc,
-                                                   uint64_t pol_in, uint64_t pol_out) {
+                                                   uint64_t pol_in, uint64_t pol_out, bool excl) {
     using Acc = typename M::acc;
     constexpr int CH = chunk_elems<In>();
     constexpr int NC = SEG / CH;
@@ -684,8 +700,9 @@ __device__ __forceinline__ void segment_scan_store(const In* src, Out* dst, int 
                 Out o[CH];
 #pragma unroll
                 for (int q = 0; q < CH; ++q) {
+                    const typename M::P before = acc;
                     acc = M::combine(acc, M::lift(convert<Acc>(raw_get<In>(r[u], q))));
-                    o[q] = convert<Out>(M::value(acc));
+                    o[q] = convert<Out>(M::value(excl ? before : acc));
                 }
                 store_chunk<Out, CH>(dst + (c0 + u) * CH, o, pol_out);
             }
@@ -693,8 +710,9 @@ __device__ __forceinline__ void segment_scan_store(const In* src, Out* dst, int 
         return;
     }
     for (int i = 0; i < n; ++i) {
+        const typename M::P before = acc;
         acc = M::combine(acc, M::lift(convert<Acc>(src[i])));
-        dst[i] = convert<Out>(M::value(acc));
+        dst[i] = convert<Out>(M::value(excl ? before : acc));
     }
 }
 
@@ -716,7 +734,7 @@ __device__ __forceinline__ void segment_scan_store(const In* src, Out* dst, int 
 template <class In, class Acc, class Out, class M, int BLOCK, int SEG>
 __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Acc)>())
     k_scan_tiles(const In* __restrict__ x, Out* __restrict__ y, int64_t len, int64_t tiles_per_line, int64_t ntiles,
-                 TileState<typename M::P> ts, ScanCtl ctl, bool has_init, Acc init) {
+                 TileState<typename M::P> ts, ScanCtl ctl, bool has_init, Acc init, bool excl) {
     using P = typename M::P;
     constexpr int W = BLOCK / kWarp;
     constexpr int64_t SUPER = (int64_t)BLOCK * SEG;
@@ -795,7 +813,7 @@ __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Ac
             const int n = (int)max((int64_t)0, min((int64_t)SEG, cnt - (int64_t)tid * SEG));
             if (n > 0)
                 segment_scan_store<In, Out, M, SEG>(x + start + (int64_t)tid * SEG, y + start + (int64_t)tid * SEG, n,
-                                                    mine, last_use, last_use);
+                                                    mine, last_use, last_use, excl);
             __syncthreads();  // warp_tot and the slot are reused next
         }
         if (k >= ntiles) break;
@@ -888,8 +906,20 @@ __device__ __forceinline__ T row_fold(const T (&run)[R]) {
 
 // Inclusive scan of a row in place, starting from the exclusive prefix
 // `mine` (absent only for the very first row of a line without init).
+// Exclusive: element i takes the fold before it, the first one `mine`
+// itself (always present: an exclusive scan starts from init).
 template <class M, class T, int R>
-__device__ __forceinline__ void row_scan_from(T (&run)[R], const typename M::P& mine) {
+__device__ __forceinline__ void row_scan_from(T (&run)[R], const typename M::P& mine, bool excl) {
+    if (excl) {
+        T a = M::value(mine);
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const T x = run[i];
+            run[i] = a;
+            a = M::op::apply(a, x);
+        }
+        return;
+    }
     T a = M::present(mine) ? M::op::apply(M::value(mine), run[0]) : run[0];
     run[0] = a;
 #pragma unroll
@@ -968,7 +998,7 @@ template <class T, class M>
 __global__ void __launch_bounds__(kWsThreads, 1)
     k_scan_tma(const __grid_constant__ CUtensorMap tin, const T* __restrict__ x, T* __restrict__ y, int64_t len,
                int64_t rows_full, int64_t tiles_per_line, int64_t ntiles, TileState<typename M::P> ts, ScanCtl ctl,
-               bool has_init, T init) {
+               bool has_init, T init, bool excl) {
     using P = typename M::P;
     constexpr int S = ws_stages<P>();
     constexpr int R = 128 / (int)sizeof(T);
@@ -1256,15 +1286,16 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             if (nt == R) {
                 T run[R];
                 row_load(run, bufs + (size_t)s * TILE_BYTES, r);
-                row_scan_from<M>(run, from);
+                row_scan_from<M>(run, from, excl);
                 row_store_global(y + row_off(s, r), run, last_use);
             } else if (nt > 0) {
                 const T* src = x + row_off(s, r);
                 T* dst = y + row_off(s, r);
                 P a = from;
                 for (int i = 0; i < nt; ++i) {
+                    const P before = a;
                     a = M::combine(a, M::lift(src[i]));
-                    dst[i] = M::value(a);
+                    dst[i] = M::value(excl ? before : a);
                 }
             }
             __syncwarp();
@@ -1277,7 +1308,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 // state is shared between blocks.
 template <class In, class Acc, class Out, class M, int ITEMS, int BLOCK>
 __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Acc)>())
-    k_scan_lines(const In* __restrict__ x, Out* __restrict__ y, int64_t len, bool has_init, Acc init) {
+    k_scan_lines(const In* __restrict__ x, Out* __restrict__ y, int64_t len, bool has_init, Acc init, bool excl,
+                 uint64_t* error_word) {
     using P = typename M::P;
     using L = RunLayout<Acc, ITEMS>;
     constexpr int W = BLOCK / kWarp;
@@ -1287,9 +1319,11 @@ __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Ac
     const int64_t start = (int64_t)blockIdx.x * len;
     const int cnt = (int)len;
     if (threadIdx.x == 0) s_prefix = has_init ? M::lift(init) : M::empty();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *error_word = 0;  // no waits here: the call's status is ok
     load_tile<In, Acc, ITEMS, BLOCK>(tile, x + start, cnt, l2_policy_evict_first());
     __syncthreads();
-    scan_apply_store<Acc, Out, M, ITEMS, BLOCK>(tile, y + start, cnt, &s_prefix, warp_tot, l2_policy_evict_first());
+    scan_apply_store<Acc, Out, M, ITEMS, BLOCK>(tile, y + start, cnt, &s_prefix, warp_tot, l2_policy_evict_first(),
+                                                excl);
 }
 
 // Lines along a strided dimension: y[i + I*(j + J*k)] over j, for every
@@ -1297,9 +1331,10 @@ __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Ac
 template <class In, class Acc, class Out, class M>
 __global__ void __launch_bounds__(256) k_scan_strided(const In* __restrict__ x, Out* __restrict__ y,
                                                       int64_t I, int64_t J, int64_t K, bool has_init,
-                                                      Acc init) {
+                                                      Acc init, bool excl, uint64_t* error_word) {
     using P = typename M::P;
     const int64_t col = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (col == 0) *error_word = 0;  // no waits here: the call's status is ok
     if (col >= I * K) return;
     const int64_t i = col % I, k = col / I;
     const In* src = x + i + I * J * k;
@@ -1313,13 +1348,15 @@ __global__ void __launch_bounds__(256) k_scan_strided(const In* __restrict__ x, 
         for (int u = 0; u < U; ++u) v[u] = src[I * (j + u)];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            const P before = acc;
             acc = M::combine(acc, M::lift(convert<Acc>(v[u])));
-            dst[I * (j + u)] = convert<Out>(M::value(acc));
+            dst[I * (j + u)] = convert<Out>(M::value(excl ? before : acc));
         }
     }
     for (; j < J; ++j) {
+        const P before = acc;
         acc = M::combine(acc, M::lift(convert<Acc>(src[I * j])));
-        dst[I * j] = convert<Out>(M::value(acc));
+        dst[I * j] = convert<Out>(M::value(excl ? before : acc));
     }
 }
 
@@ -1409,7 +1446,7 @@ ak_status launch_tma(const ScanCall& c, const ScanPlan& p) {
     if (e != cudaSuccess) return cuda_fail(e);
     k_scan_tma<T, M><<<(unsigned)grid, kWsThreads, ws_smem_bytes<typename M::P>(), c.stream>>>(
         tin, static_cast<const T*>(c.src), static_cast<T*>(c.dst), c.len, rows_full, p.tma_tiles_per_line,
-        p.tma_tiles, ts, ctl, c.has_init, init);
+        p.tma_tiles, ts, ctl, c.has_init, init, c.exclusive);
     ak_status s = check_launch();
     if (s == AK_OK) count_launches(1);
     return s;
@@ -1424,7 +1461,8 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
         const int64_t cols = c.inner * c.outer;
         const unsigned blocks = (unsigned)((cols + 255) / 256);
         k_scan_strided<In, Acc, Out, M><<<blocks, 256, 0, c.stream>>>(
-            static_cast<const In*>(c.src), static_cast<Out*>(c.dst), c.inner, c.len, c.outer, c.has_init, init);
+            static_cast<const In*>(c.src), static_cast<Out*>(c.dst), c.inner, c.len, c.outer, c.has_init, init,
+            c.exclusive, static_cast<uint64_t*>(c.ws));
         ak_status s = check_launch();
         if (s == AK_OK) count_launches(1);
         return s;
@@ -1459,7 +1497,8 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
             auto lines = [&](auto blk) {
                 constexpr int B = decltype(blk)::value;
                 k_scan_lines<In, Acc, Out, M, ITEMS, B><<<(unsigned)p.tiles, B, 0, c.stream>>>(
-                    static_cast<const In*>(c.src), static_cast<Out*>(c.dst), c.len, c.has_init, init);
+                    static_cast<const In*>(c.src), static_cast<Out*>(c.dst), c.len, c.has_init, init, c.exclusive,
+                    reinterpret_cast<uint64_t*>(ws));
             };
             if (c.len <= 64 * ITEMS) lines(std::integral_constant<int, 64>{});
             else if (c.len <= 128 * ITEMS || BLOCK == 128) lines(std::integral_constant<int, 128>{});
@@ -1481,12 +1520,68 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
             if (e != cudaSuccess) return cuda_fail(e);
             k_scan_tiles<In, Acc, Out, M, BLOCK, SEG><<<(unsigned)grid, BLOCK, 0, c.stream>>>(
                 static_cast<const In*>(c.src), static_cast<Out*>(c.dst), c.len, p.tiles_per_line, p.tiles, ts, ctl,
-                c.has_init, init);
+                c.has_init, init, c.exclusive);
         }
         ak_status s = check_launch();
         if (s == AK_OK) count_launches(1);
         return s;
     }
+}
+
+// The scan plan from the accumulator and partial sizes: kernel kind, run
+// length and block, tile counts and workspace. tma_type: the element type
+// may take the TMA tile scan (one 4- or 8-byte type throughout, f32 / i32 /
+// i64 with a neutral element: f64 additions run on the FP64 pipe, the matrix
+// product spends more operator work per byte and Optional partials more per
+// combine; those run faster as super-tiles, whose blocks carry more warps per
+// SM); it then also needs rows of 128 bytes, several tiles per line, and
+// lines that start on a row boundary unless there is only one.
+inline ak_status plan_sizes(int64_t inner, int64_t len, int64_t outer, size_t asz, size_t psz, bool tma_type,
+                            int items, ScanPlan* p) {
+    p->state_off = kWsHeader;
+    p->ws_bytes = kWsHeader;
+    p->tiles = 0;
+    p->tiles_per_line = 0;
+    p->grid = 0;
+    p->tma = false;
+    p->tma_tiles_per_line = 0;
+    p->tma_tiles = 0;
+    p->tma_ws_bytes = 0;
+    if (inner > 1) {
+        p->kind = 1;
+        p->block = 256;
+        p->items = 1;
+        return AK_OK;
+    }
+    p->kind = 0;
+    const int it = asz >= 16 ? 8 : (asz == 8 ? 16 : 32);
+    if (items != 0 && items != it) return AK_ERR_UNSUPPORTED;
+    p->items = it;
+    const int block = asz >= 16 ? 128 : 256;
+    const int seg = asz >= 16 ? 64 : (asz == 8 ? 64 : 32);
+    p->block = block;
+    const int64_t tile = (int64_t)block * it;
+    if (len <= tile) {
+        p->kind = 2;  // every line fits one tile: no state shared between blocks
+        p->tiles_per_line = 1;
+        p->tiles = outer;
+        return AK_OK;
+    }
+    const int64_t super = (int64_t)block * seg;
+    p->tiles_per_line = (len + super - 1) / super;
+    p->tiles = p->tiles_per_line * outer;
+    p->ws_bytes = align_up(kWsHeader + (size_t)p->tiles * (16 + align_up(psz, 16)), 256);  // TileRec per super-tile
+    const int64_t rl = 128 / (int64_t)asz;
+    if (items == 0 && tma_type && (asz == 4 || asz == 8) && len > kWsRows * rl && (outer == 1 || len % rl == 0) &&
+        len / rl < ((int64_t)1 << 31) && outer < ((int64_t)1 << 31)) {
+        const int64_t rows = (len + rl - 1) / rl;
+        p->tma = true;
+        p->tma_tiles_per_line = (rows + kWsRows - 1) / kWsRows;
+        p->tma_tiles = p->tma_tiles_per_line * outer;
+        p->tma_ws_bytes = align_up(kWsHeader + (size_t)p->tma_tiles * (16 + align_up(psz, 16)), 256);
+        p->ws_bytes = std::max(p->ws_bytes, p->tma_ws_bytes);
+    }
+    return AK_OK;
 }
 
 // Runs a scan whose input type is In: dispatches the accumulator / output

@@ -38,7 +38,7 @@ def test_status_strings_and_sizes(L):
     for s in range(7):
         assert L.ak_status_string(s)
     assert L.ak_status_string(99) == b"unknown status"
-    assert [L.ak_dtype_size(t) for t in range(6)] == [4, 8, 2, 4, 8, 16]
+    assert [L.ak_dtype_size(t) for t in range(7)] == [4, 8, 2, 4, 8, 16, 1]
     assert L.ak_dtype_size(17) == 0
 
 
@@ -48,7 +48,7 @@ def test_opts_default(L):
     o.no_neutral = 7
     L.ak_opts_default(ctypes.byref(o))
     assert o.no_neutral == 0 and o.dims_shape == 0 and o.debug_skip_publish_tile == -1
-    assert ctypes.sizeof(_abi.ak_opts) == 40
+    assert ctypes.sizeof(_abi.ak_opts) == 48 and o.exclusive == 0 and o.reserved == 0
 
 
 def _reduce(L, src=0x1000, n=10, in_t=0, f=0, op=0, acc=0, out=0, init=None, mode=0, dst=0x2000, host=None):
@@ -76,14 +76,15 @@ def test_reduce_validates_before_device(L):
 def test_reduce_dims_validates_before_device(L):
     from mapreduce_prefix_scan_gb300._abi import AK_ERR_INVALID_ARG as INV
     sh = (ctypes.c_int64 * 3)(4, 5, 6)
-    call = lambda ndim=3, shape=sh, mask=2, mode=0, init=None: L.ak_reduce_dims(
-        0x1000, ndim, shape, mask, 0, 0, 0, 0, 0, init, mode, 0x2000, 0x4000, 1 << 20, None, None)
+    call = lambda ndim=3, shape=sh, mask=2, mode=0, init=None, strides=None: L.ak_reduce_dims(
+        0x1000, ndim, shape, strides, mask, 0, 0, 0, 0, 0, init, mode, 0x2000, 0x4000, 1 << 20, None, None)
     assert call(ndim=0) == INV
     assert call(ndim=9) == INV
     assert call(mask=1 << 3) == INV
     assert call(shape=None) == INV
     assert call(shape=(ctypes.c_int64 * 3)(4, -1, 6)) == INV
     assert call(mode=1) == INV
+    assert call(strides=(ctypes.c_int64 * 3)(1, -4, 20)) == INV   # negative strides are refused
 
 
 def test_accumulate_validates_and_plans_on_host(L):
@@ -96,6 +97,15 @@ def test_accumulate_validates_and_plans_on_host(L):
     assert acc(src=None) == INV
     assert acc(dst=0x1000 + 64) == INV        # partial overlap
     assert acc(in_t=5, a=5, o=5, op=0) == UNS
+    from mapreduce_prefix_scan_gb300 import _abi
+    for field, bad in (("exclusive", 2), ("exclusive", -1), ("reserved", 1)):
+        o = _abi.ak_opts()
+        L.ak_opts_default(ctypes.byref(o))
+        setattr(o, field, bad)
+        assert L.ak_accumulate(0x1000, 0x800000, 2, sh, 0, 0, 0, 0, 0, None, 0x4000, 1 << 20,
+                               ctypes.byref(o), None) == INV
+    assert L.ak_scan_status(None) == INV
+    assert L.ak_scan_status(0x4001) == INV
     b = ctypes.c_size_t()
     # whole-array f64 scan of 1e8: super-tiles of 256 threads x 64 elements,
     # one 32-byte state record each (tag, check word, value)
@@ -110,12 +120,13 @@ def test_accumulate_validates_and_plans_on_host(L):
 
 def test_dims_selector(L):
     import mapreduce_prefix_scan_gb300 as ak
-    # 3072 x 2048 bf16, dims=2 (12.6 MB): 16-byte vectors of 8, 16 threads
-    # across a 128-output row segment, 16 row groups, the reduction split 16
-    # ways and the split blocks of an output tile combined in a thread-block
-    # cluster (small inputs)
+    # 3072 x 2048 bf16, dims=2 (12.6 MB, latency-bound): 16-byte vectors of 8,
+    # 8 threads across a 64-output row segment, 32 row groups of 4 rows, the
+    # reduction split 16 ways and the split blocks of an output tile combined
+    # in a thread-block cluster: 768 blocks of 16 KB
     shape, tile, groups, split = ak.ak_dims_select(3072, 2048, 1, 2, 8, 152)
-    assert shape == "columns" and tile == 128 and groups == 16 and split == 16
+    assert shape == "columns" and tile == 64 and groups == 32 and split == 16
+    assert (3072 // tile) * split == 768 and 2048 // (split * groups) == 4
     # a larger input: a warp across a 256-output row segment, 8 row groups,
     # split through the workspace and a second pass, >= 1 block per SM
     shape, tile, groups, split = ak.ak_dims_select(3072, 8192, 1, 2, 8, 152)
@@ -144,3 +155,25 @@ def test_missing_library_fails_loudly():
     r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0
     assert "libak.so not built" in r.stderr
+
+
+def test_findall_validates_and_plans_on_host(L):
+    from mapreduce_prefix_scan_gb300._abi import AK_ERR_INVALID_ARG as INV, AK_ERR_UNSUPPORTED as UNS
+    cnt = ctypes.c_int64()
+    call = lambda src=0x1000, n=100, t=6, idx=0x8000, cd=0x9000, ch=None: L.ak_findall(
+        src, n, t, idx, cd, ch, 0x4000, 1 << 20, None, None)
+    assert call(n=-1) == INV
+    assert call(t=9) == INV
+    assert call(cd=None, ch=None) == INV
+    assert call(src=None) == INV
+    assert call(idx=None) == INV
+    assert call(idx=0x8004) == INV          # int64 indices need 8-byte alignment
+    assert call(src=0x1002, t=0) == INV     # misaligned f32 source
+    assert call(t=2) == UNS                 # bf16
+    assert call(t=5) == UNS                 # matrices
+    # empty input: count 0 on the host, nothing launched
+    assert L.ak_findall(None, 0, 6, None, None, ctypes.byref(cnt), None, 0, None, None) == 0 and cnt.value == 0
+    # one 32-byte record per tile of 16 K flags, after the 256-byte header
+    b = ctypes.c_size_t()
+    assert L.ak_findall_workspace_size(10**8, 6, None, ctypes.byref(b)) == 0
+    assert b.value >= 256 + (-(-10**8 // 16384)) * 32 + 8

@@ -97,3 +97,4 @@ def test_noalloc_host_result_and_empty():
         assert st == 0 and out.value == 100_000 * 100_001 // 2
     st = L.ak_reduce_noalloc(None, 0, D["i64"], 0, 2, D["i64"], D["i64"], None, 0, None, ctypes.byref(out), None, s)
     assert st == _abi.AK_ERR_EMPTY_NO_INIT
+
