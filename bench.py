@@ -154,7 +154,7 @@ def _traffic_from_profile(kernel_hash: str, algorithmic_bytes: float):
 
 def _kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("reduce.cu", "ak_common.cuh", "ak_types.cuh"):
+    for name in ("reduce.cuh", "ak_common.cuh", "ak_types.cuh"):
         with open(os.path.join(ROOT, "mapreduce_prefix_scan_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -167,8 +167,14 @@ def _flush_l2(buf):
     buf[: buf.numel() // 2].sum()
 
 
-def _time_call(fn, reps, flush_buf, torch):
-    """Median / min microseconds of fn() with the L2 flushed before each call."""
+def _time_call(fn, reps, flush_buf, torch, host_sync=False):
+    """Median / min microseconds of fn() with the L2 flushed before each call.
+
+    GPU time only: a spin of about 100 us is queued on the stream before the
+    start event, so the call's host work (argument marshalling, the plan)
+    is done and its kernels are queued by the time the event fires. A call
+    that synchronizes on the host (host_sync: a host result) cannot be
+    queued ahead; it is timed as the user sees it, host work included."""
     s = torch.cuda.current_stream()
     ts = []
     for _ in range(3):
@@ -177,6 +183,8 @@ def _time_call(fn, reps, flush_buf, torch):
         _flush_l2(flush_buf)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        if not host_sync:
+            torch.cuda._sleep(200_000)
         e0.record(s)
         fn()
         e1.record(s)
@@ -238,8 +246,8 @@ def _configs(ak, torch, dev, peak, flush_buf, reps):
     out = {}
     l2_twice = 2 * 129 * 2**20
 
-    def rec(name, make_fn, x, nbytes):
-        med, mn = _time_call(make_fn(x), reps, flush_buf, torch)
+    def rec(name, make_fn, x, nbytes, host_sync=False):
+        med, mn = _time_call(make_fn(x), reps, flush_buf, torch, host_sync=host_sync)
         in_bytes = x.numel() * x.element_size()
         copies = max(1, min(64, -(-l2_twice // in_bytes)))
         xs = [x] + [x.clone() for _ in range(copies - 1)]
@@ -260,7 +268,19 @@ def _configs(ak, torch, dev, peak, flush_buf, reps):
     ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
     rec("sum_f32_1e6_device", lambda a: (lambda: ak.ak_reduce(a, dst=r, init=0.0, workspace=ws)), x, 4 * 10**6 + 4)
     rec("sum_f32_1e6_host", lambda a: (lambda: ak.ak_reduce(a, to_host=True, init=0.0, workspace=ws)), x,
-        4 * 10**6 + 4)
+        4 * 10**6 + 4, host_sync=True)
+    # the same host result through the C ABI with prepared arguments (no
+    # Python marshalling): the library's own time, synchronization included
+    L = ak.lib()
+    D = ak.DTYPES
+    hres = __import__("ctypes").c_float()
+    hinit = __import__("ctypes").c_float(0.0)
+    href = __import__("ctypes").byref
+    sp = torch.cuda.current_stream().cuda_stream
+    rec("sum_f32_1e6_host_cabi", lambda a: (lambda: L.ak_reduce(a.data_ptr(), a.numel(), D["f32"], 0, 0, D["f32"],
+                                                                 D["f32"], href(hinit), 1, None, href(hres),
+                                                                 ws.data_ptr(), ws.numel(), None, sp)),
+        x, 4 * 10**6 + 4, host_sync=True)
     rec("sum_i32_1e6_device", lambda a: (lambda: ak.ak_reduce(a, dst=ri, workspace=ws)), xi, 4 * 10**6 + 4)
     del x, xi
     # strided dims=2 reductions
@@ -291,8 +311,32 @@ def _configs(ak, torch, dev, peak, flush_buf, reps):
         w = torch.empty(wsz, dtype=torch.uint8, device=dev)
         rec(name, lambda t: (lambda: ak.ak_accumulate(t, dst=y, workspace=w, **kw)), a, nbytes)
 
+    # contiguous dims=1 reduction (a warp per output, k_dims_rows)
+    a = torch.from_numpy(synth.normal_f32(4096 * 4096, 0, 41)).reshape(4096, 4096).to(dev)
+    dst1 = torch.empty(4096, dtype=torch.float32, device=dev)
+    rec("dims1_4096x4096_f32", lambda t: (lambda: ak.ak_reduce_dims(t, [0], dst=dst1, workspace=ws)), a,
+        4096 * 4096 * 4 + 4096 * 4)
+    del a
+    # fused two-source reduction: the dot product of two 1e8 f32 arrays
+    xa = torch.from_numpy(synth.uniform_f32_pm1(N_BIG, 0, 100)).to(dev)
+    xb = torch.from_numpy(synth.uniform_f32_pm1(N_BIG, 0, 101)).to(dev)
+    rd = torch.empty(1, dtype=torch.float32, device=dev)
+    rec("dot_f32_1e8", lambda t: (lambda: ak.ak_reduce2(t, xb, f="mul", dst=rd, workspace=ws)), xa, 8 * N_BIG + 4)
+    del xa, xb
+    # findall over 1e8 Bool flags, half of them set: n bytes read, 8 per index written
+    w = synth.words(N_BIG, 0, 90)
+    fl = torch.from_numpy(((w >> np.uint64(63)) == 1).astype(np.uint8)).to(dev)
+    del w
+    nset = int(fl.sum().item())
+    idx = torch.empty(N_BIG, dtype=torch.int64, device=dev)
+    cnt = torch.empty(1, dtype=torch.int64, device=dev)
+    fws = torch.empty(ak.ak_findall_workspace_size(N_BIG, "u8"), dtype=torch.uint8, device=dev)
+    rec("findall_u8_1e8_half", lambda t: (lambda: ak.ak_findall(t, idx=idx, count=cnt, to_host=False, workspace=fws)),
+        fl, N_BIG + 8 * nset + 8)
+    del fl, idx
     scan_rec("cumsum_f64_1e8", synth.uniform_f64_01(N_BIG, 0, 60), (N_BIG,), 16 * N_BIG)
     scan_rec("cumsum_f32_1e8", synth.normal_f32(N_BIG, 0, 65), (N_BIG,), 8 * N_BIG)
+    scan_rec("exclusive_cumsum_f32_1e8", synth.normal_f32(N_BIG, 0, 65), (N_BIG,), 8 * N_BIG, exclusive=True)
     scan_rec("accumulate_max_optional_f32_1e7", synth.normal_f32(10**7, 0, 61), (10**7,), 8 * 10**7, op="max",
              opts=ak.make_opts(no_neutral=True))
     scan_rec("cumsum_dims1_4096x4096_f32", synth.normal_f32(4096 * 4096, 0, 62), (4096, 4096), 8 * 4096 * 4096,
@@ -571,6 +615,20 @@ def run_profile(case: str):
         x = torch.from_numpy(synth.normal_bf16_bits(3072 * 2048, 0, 40).view(np.int16)).view(torch.bfloat16)
         x = x.reshape(2048, 3072).to(dev)
         fn = lambda: ak.ak_reduce_dims(x, [1])
+    elif case == "scan_lines":  # cumsum along dims=1 of 4096 x 4096 f32: lines that fit one tile
+        x = torch.from_numpy(synth.normal_f32(4096 * 4096, 0, 62)).reshape(4096, 4096).to(dev)
+        y = torch.empty_like(x)
+        fn = lambda: ak.ak_accumulate(x, dst=y, dim=0)
+    elif case == "scan_lines_mat2":  # prefix products along dims=1 of 1024 x 8192 matrices
+        x = torch.from_numpy(synth.mat2_modp(1024 * 8192, 0, 64)).reshape(8192, 1024, 4).to(dev)
+        y = torch.empty_like(x)
+        fn = lambda: ak.ak_accumulate(x, dst=y, dim=0, op="matmul", elem="mat2")
+    elif case == "findall":  # 1e8 Bool flags, half set
+        w = synth.words(10**8, 0, 90)
+        x = torch.from_numpy(((w >> np.uint64(63)) == 1).astype(np.uint8)).to(dev)
+        idx = torch.empty(10**8, dtype=torch.int64, device=dev)
+        cnt = torch.empty(1, dtype=torch.int64, device=dev)
+        fn = lambda: ak.ak_findall(x, idx=idx, count=cnt, to_host=False)
     elif case == "dims_big":  # 8192 x 8192 f32, sum(x; dims=2)
         x = torch.from_numpy(synth.normal_f32(8192 * 8192, 0, 40)).reshape(8192, 8192).to(dev)
         fn = lambda: ak.ak_reduce_dims(x, [1])
@@ -592,7 +650,8 @@ def main():
     ap.add_argument("--config-reps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--small", action="store_true", help="n = 1e6 (quick runs)")
-    ap.add_argument("--profile", default=None, help="run a small ncu case: reduce|scan|scan_f32|scan_max|scan_mat2|dims|dims_big")
+    ap.add_argument("--profile", default=None, help="run a small ncu case: reduce|scan|scan_f32|scan_max|scan_mat2|"
+                    "scan_lines|scan_lines_mat2|findall|dims|dims_big")
     args = ap.parse_args()
     if args.profile:
         run_profile(args.profile)

@@ -168,9 +168,13 @@ uint64_t ak_kernel_launch_count(void);
  *   src        device, n elements of `in` (n == 0 allowed)
  *   dst_dev    device, one element of `out`, or NULL
  *   dst_host   host, one element of `out`, or NULL; when given the call
- *              copies the result back and synchronizes `stream` (with
+ *              synchronizes `stream` and returns the result there (with
  *              AK_STORE_FOLD, *dst_host holds R_old on entry, unless dst_dev
- *              is also given, in which case R is the device element)
+ *              is also given, in which case R is the device element). The
+ *              last pass writes the bare partial straight into a small
+ *              mapped, pinned host slot of the calling thread (64 bytes,
+ *              allocated by its first host-result call and kept until the
+ *              process exits), and the host finishes it.
  *   At least one of dst_dev / dst_host must be non-NULL.
  * Empty input: AK_STORE_INIT stores init; AK_STORE_FOLD leaves R unchanged;
  *   AK_STORE_OVERWRITE stores the neutral element of op (0 for +, 1 for *,

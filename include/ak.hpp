@@ -144,8 +144,10 @@ ak_status accumulate_workspace_size(int64_t n, size_t* bytes) {
     static_assert(user::supported<T>(), "T: trivially copyable, 4, 8 or 16 bytes");
     using M = monoid_of<Op, T>;
     if (!bytes || n < 0) return AK_ERR_INVALID_ARG;
+    const bool o_single_pass = false;
     ScanPlan p;
-    const ak_status s = scan::plan_sizes(1, n, 1, sizeof(T), sizeof(typename M::P), tma_eligible<T, Op>(), 0, &p);
+    const ak_status s = scan::plan_sizes(1, n, 1, sizeof(T), sizeof(typename M::P), tma_eligible<T, Op>(), 0, &p, sizeof(T),
+                                          o_single_pass);
     if (s != AK_OK) return s;
     *bytes = p.ws_bytes;
     return AK_OK;
@@ -170,8 +172,10 @@ ak_status accumulate(const T* src, T* dst, int64_t n, const T* init, bool exclus
     ak_opts_default(&o);
     if (opts) o = *opts;
     if (o.wait_limit_ns <= 0) o.wait_limit_ns = 1000000000LL;
+    const bool o_single_pass = o.debug_skip_publish_tile >= 0;  // fault injection needs the single-pass waits
     ScanPlan p;
-    ak_status s = scan::plan_sizes(1, n, 1, sizeof(T), sizeof(typename M::P), tma_eligible<T, Op>(), 0, &p);
+    ak_status s = scan::plan_sizes(1, n, 1, sizeof(T), sizeof(typename M::P), tma_eligible<T, Op>(), 0, &p, sizeof(T),
+                                          o_single_pass);
     if (s != AK_OK) return s;
     if (!workspace || workspace_bytes < p.ws_bytes || reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
         return AK_ERR_WORKSPACE;

@@ -157,6 +157,12 @@ struct ReducePlan {
 ak_status plan_reduce(int64_t n, ak_dtype in, ak_dtype acc, bool no_neutral, int target_blocks,
                       const DeviceInfo& dev, ReducePlan* plan);
 ak_status run_reduce(const ReduceCall& c, const ReducePlan& plan);
+// The whole-array entry behind ak_reduce / ak_reduce2 / ak_reduce_noalloc
+// (api.cu): validation, empty rules, launch, host finish. host_slot: a host
+// result may use the calling thread's pinned host slot.
+ak_status reduce_entry(const void* src, const void* src2, int map2, int64_t n, ak_dtype in, ak_map f, ak_op op,
+                       ak_dtype acc, ak_dtype out, const void* init, ak_store mode, void* dst_dev, void* dst_host,
+                       void* ws, size_t ws_bytes, const ak_opts* opts, void* stream, bool host_slot);
 
 // Canonical strided problem: out[i + inner*k] = fold_j x[i + ldj*j + ldk*k]
 // (a dense array has ldj = inner, ldk = inner*red).
@@ -231,10 +237,15 @@ struct ScanPlan {
     bool tma;
     int64_t tma_tiles_per_line, tma_tiles;
     size_t tma_ws_bytes;
+    // kind 0, one line that fits L2 (not TMA): reduce-then-scan in three
+    // launches; workspace offsets of the segment totals, tile aggregates and
+    // tile prefixes
+    bool three;
+    size_t seg_off, agg_off, pre_off;
 };
 ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_dtype acc, ak_dtype out,
                     ak_op op, bool no_neutral, int target_blocks, int items,
-                    const DeviceInfo& dev, ScanPlan* plan);
+                    const DeviceInfo& dev, ScanPlan* plan, bool single_pass = false);
 ak_status run_scan(const ScanCall& c, const ScanPlan& plan);
 
 // findall: tiles and workspace; the kernel of findall.cu.

@@ -238,10 +238,44 @@ extern "C" ak_status ak_reduce_workspace_size(int64_t n, ak_dtype in, ak_dtype a
     return AK_OK;
 }
 
-// ak_reduce and ak_reduce2: one source, or a fused element f(src[i], src2[i]).
-static ak_status reduce_impl(const void* src, const void* src2, int map2, int64_t n, ak_dtype in, ak_map f,
-                             ak_op op, ak_dtype acc, ak_dtype out, const void* init, ak_store mode, void* dst_dev,
-                             void* dst_host, void* ws, size_t ws_bytes, const ak_opts* opts, void* stream) {
+// A per-thread slot of mapped, pinned host memory for host results: the
+// finishing kernel writes the bare partial straight into it (no copy to
+// enqueue, no staging of a pageable buffer), and the host reads it after the
+// stream synchronizes. Allocated on a thread's first host-result call and
+// kept until the process exits (64 bytes). Null when the allocation fails:
+// the caller then copies through the workspace.
+static unsigned char* host_result_slot(void** dev_ptr) {
+    struct Slot {
+        unsigned char* host = nullptr;
+        void* dev = nullptr;
+        bool tried = false;
+    };
+    static thread_local Slot slot;
+    if (!slot.tried) {
+        slot.tried = true;
+        void* h = nullptr;
+        if (cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable) == cudaSuccess) {
+            void* d = nullptr;
+            if (cudaHostGetDevicePointer(&d, h, 0) == cudaSuccess) {
+                slot.host = static_cast<unsigned char*>(h);
+                slot.dev = d;
+            } else {
+                cudaFreeHost(h);
+            }
+        }
+        cudaGetLastError();
+    }
+    *dev_ptr = slot.dev;
+    return slot.host;
+}
+
+// ak_reduce, ak_reduce2 and ak_reduce_noalloc: one source, or a fused
+// element f(src[i], src2[i]). host_slot: a host result may go through the
+// calling thread's pinned slot (not for callers that must not allocate).
+ak_status ak::reduce_entry(const void* src, const void* src2, int map2, int64_t n, ak_dtype in, ak_map f,
+                           ak_op op, ak_dtype acc, ak_dtype out, const void* init, ak_store mode, void* dst_dev,
+                           void* dst_host, void* ws, size_t ws_bytes, const ak_opts* opts, void* stream,
+                           bool host_slot) {
     ak_status s = check_types(in, f, op, acc, out);
     if (s != AK_OK) return s;
     if (n < 0 || (n > 0 && !src) || (!dst_dev && !dst_host)) return AK_ERR_INVALID_ARG;
@@ -309,6 +343,12 @@ static ak_status reduce_impl(const void* src, const void* src2, int map2, int64_
     c.init = ini;
     c.dst = dst_dev;
     c.bare = dst_dev ? nullptr : static_cast<char*>(ws) + plan.bare_off;
+    unsigned char* slot = nullptr;
+    if (!dst_dev && host_slot) {
+        void* slot_dev = nullptr;
+        slot = host_result_slot(&slot_dev);
+        if (slot) c.bare = slot_dev;
+    }
     c.ws = ws;
     c.ws_bytes = ws_bytes;
     c.target_blocks = o.target_blocks;
@@ -321,6 +361,13 @@ static ak_status reduce_impl(const void* src, const void* src2, int map2, int64_
             cudaError_t e = cudaMemcpyAsync(dst_host, dst_dev, ak_dtype_size(out), cudaMemcpyDeviceToHost, st);
             if (e != cudaSuccess) return cuda_fail(e);
             return sync_and_check(st);
+        }
+        if (slot) {
+            s = sync_and_check(st);
+            if (s != AK_OK) return s;
+            alignas(16) unsigned char bare[32];
+            memcpy(bare, slot, sizeof bare);
+            return host_finish(bare, in, acc, out, op, no_neutral, mode, ini, dst_host);
         }
         const size_t psz = partial_size(acc, no_neutral);
         alignas(16) unsigned char bare[32];
@@ -337,8 +384,8 @@ static ak_status reduce_impl(const void* src, const void* src2, int map2, int64_
 extern "C" ak_status ak_reduce(const void* src, int64_t n, ak_dtype in, ak_map f, ak_op op, ak_dtype acc,
                                ak_dtype out, const void* init, ak_store mode, void* dst_dev, void* dst_host,
                                void* ws, size_t ws_bytes, const ak_opts* opts, void* stream) {
-    return reduce_impl(src, nullptr, 0, n, in, f, op, acc, out, init, mode, dst_dev, dst_host, ws, ws_bytes, opts,
-                       stream);
+    return reduce_entry(src, nullptr, 0, n, in, f, op, acc, out, init, mode, dst_dev, dst_host, ws, ws_bytes, opts,
+                        stream, true);
 }
 
 extern "C" ak_status ak_reduce2(const void* src_a, const void* src_b, int64_t n, ak_dtype in, ak_map2 f,
@@ -348,8 +395,8 @@ extern "C" ak_status ak_reduce2(const void* src_a, const void* src_b, int64_t n,
     if (n > 0 && !src_b) return AK_ERR_INVALID_ARG;
     // a fused element needs a second source even when n == 0 decides nothing
     const void* b = src_b ? src_b : reinterpret_cast<const void*>(uintptr_t(256));
-    return reduce_impl(src_a, b, (int)f, n, in, AK_MAP_IDENTITY, op, acc, out, init, mode, dst_dev, dst_host, ws,
-                       ws_bytes, opts, stream);
+    return reduce_entry(src_a, b, (int)f, n, in, AK_MAP_IDENTITY, op, acc, out, init, mode, dst_dev, dst_host, ws,
+                        ws_bytes, opts, stream, true);
 }
 
 // ===========================================================================
@@ -655,7 +702,9 @@ extern "C" ak_status ak_accumulate(const void* src, void* dst, int ndim, const i
     DeviceInfo dev;
     if (!current_device(&dev)) return AK_ERR_CUDA;
     ScanPlan p;
-    s = plan_scan(inner, len, outer, in, acc, out, op, o.no_neutral != 0, o.target_blocks, o.items_per_thread, dev, &p);
+    // fault injection targets the single-pass kernels' bounded waits
+    s = plan_scan(inner, len, outer, in, acc, out, op, o.no_neutral != 0, o.target_blocks, o.items_per_thread, dev, &p,
+                  o.debug_skip_publish_tile >= 0);
     if (s != AK_OK) return s;
     if (!ws || ws_bytes < p.ws_bytes || !aligned(ws, 16)) return AK_ERR_WORKSPACE;
     ScanCall c;

@@ -76,12 +76,13 @@ static void select_shape(int64_t I, int64_t J, int64_t K, int esz, int vec, int 
     if (shape == AK_SHAPE_COLUMNS && cluster_ok) {
         // Prefer a cluster split (2..16 blocks per output tile, partials
         // combined in distributed shared memory): try row segments of 32,
-        // 16, 8 and 4 threads until the wanted split fits a cluster. These
-        // inputs are latency-bound: aim at about 16 KB a block (4 rows of
-        // 16-byte loads in flight per thread), the size at which a plain
-        // read of a 12.6 MB array was fastest on GB300.
-        const int64_t per_block_c = (int64_t)kBlock * 4 * 16;
-        const int64_t target_c = std::max<int64_t>(sm_count, std::min<int64_t>((int64_t)sm_count * 8,
+        // 16, 8 and 4 threads until the wanted split fits a cluster. The
+        // whole grid must be resident at once (a cluster that waits for a
+        // second wave doubles the time of these latency-bound sizes): one
+        // round of kUnroll 16-byte rows per thread, at most 4 blocks per SM
+        // (the kernel's register budget).
+        const int64_t per_block_c = (int64_t)kBlock * dims::kUnroll * 16;
+        const int64_t target_c = std::max<int64_t>(sm_count, std::min<int64_t>((int64_t)sm_count * 4,
                                                                                (bytes + per_block_c - 1) / per_block_c));
         for (int tpr : {32, 16, 8, 4}) {
             if (tpr > vecs_per_row && tpr != 4) continue;

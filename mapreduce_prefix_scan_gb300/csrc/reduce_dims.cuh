@@ -92,14 +92,17 @@ struct RowSeg {
 // pass. Otherwise blockIdx.y is the split index and split > 1 writes
 // partials for k_dims_finish.
 template <class In, class Acc, class Out, class Map, class M, int VB, bool CLUSTER>
-__global__ void __launch_bounds__(kBlock, CLUSTER ? 6 : 4) k_dims_strided(const In* __restrict__ x, int64_t I, int64_t J,
+__global__ void __launch_bounds__(kBlock, 4) k_dims_strided(const In* __restrict__ x, int64_t I, int64_t J,
                                                          int64_t K, int64_t ldj, int64_t ldk, int tile_out, int tpr,
                                                          int R,
                                                          int split, typename M::P* __restrict__ partials,
                                                          DimsStore<Acc, Out, M> st) {
     using P = typename M::P;
     constexpr int V = VB / (int)sizeof(In);
-    __shared__ P smem[kBlock * V];
+    // row-group partials, row groups tile_out + 1 apart (an odd pitch: the
+    // stores of a warp's row groups and the fold's reads spread over banks)
+    __shared__ P smem[kBlock * V + kBlock];
+    const int pitch = tile_out + 1;
 
     const int64_t tiles_i = div_fast(I + tile_out - 1, tile_out);
     const int64_t tile_id = CLUSTER ? blockIdx.x / split : blockIdx.x;
@@ -121,28 +124,28 @@ __global__ void __launch_bounds__(kBlock, CLUSTER ? 6 : 4) k_dims_strided(const 
         const In* base = x + i0 + ldk * k;
         if (i0 + V <= I) {
             // ROWS rows per round, all loads issued before any is used; a
-            // short last round is predicated, not walked row by row. The
-            // cluster plans (small inputs) give each group about 4 rows.
-            constexpr int ROWS = CLUSTER ? 4 : kUnroll;
-            int64_t j = jr;
-            for (; j + ROWS <= jre; j += ROWS) {
+            // short last round is predicated, not walked row by row
+            constexpr int ROWS = kUnroll;
+            const In* p = base + ldj * jr;     // walks the rows by pointer
+            int left = (int)(jre - jr);        // rows of this group (< 2^31)
+            for (; left >= ROWS; left -= ROWS, p += ldj * ROWS) {
                 RowSeg<In, VB> r[ROWS];
 #pragma unroll
-                for (int u = 0; u < ROWS; ++u) r[u].load(base + ldj * (j + u));
+                for (int u = 0; u < ROWS; ++u) r[u].load(p + ldj * u);
 #pragma unroll
                 for (int u = 0; u < ROWS; ++u)
 #pragma unroll
                     for (int q = 0; q < V; ++q)
                         acc[q] = M::combine(acc[q], lift_elem<In, Acc, Map, M>(r[u].get(q)));
             }
-            if (j < jre) {
+            if (left > 0) {
                 RowSeg<In, VB> r[ROWS];
 #pragma unroll
                 for (int u = 0; u < ROWS; ++u)
-                    if (j + u < jre) r[u].load(base + ldj * (j + u));
+                    if (u < left) r[u].load(p + ldj * u);
 #pragma unroll
                 for (int u = 0; u < ROWS; ++u)
-                    if (j + u < jre)
+                    if (u < left)
 #pragma unroll
                         for (int q = 0; q < V; ++q)
                             acc[q] = M::combine(acc[q], lift_elem<In, Acc, Map, M>(r[u].get(q)));
@@ -160,7 +163,7 @@ __global__ void __launch_bounds__(kBlock, CLUSTER ? 6 : 4) k_dims_strided(const 
     // smem[rg][c*V + q]; group rows are contiguous ranges, combined in order
     if (rg < R) {
 #pragma unroll
-        for (int q = 0; q < V; ++q) smem[rg * tile_out + c * V + q] = acc[q];
+        for (int q = 0; q < V; ++q) smem[rg * pitch + c * V + q] = acc[q];
     }
     __syncthreads();
     if (kBlock % tile_out != 0) {
@@ -170,7 +173,7 @@ __global__ void __launch_bounds__(kBlock, CLUSTER ? 6 : 4) k_dims_strided(const 
             const int64_t i = ct * tile_out + o;
             if (i >= I) continue;
             P a = smem[o];
-            for (int g = 1; g < R; ++g) a = M::combine(a, smem[g * tile_out + o]);
+            for (int g = 1; g < R; ++g) a = M::combine(a, smem[g * pitch + o]);
             if (split == 1) dims_store<Acc, Out, M>(a, st, i + I * k);
             else if constexpr (!CLUSTER) partials[((int64_t)s * K + k) * I + i] = a;
         }
@@ -187,8 +190,8 @@ __global__ void __launch_bounds__(kBlock, CLUSTER ? 6 : 4) k_dims_strided(const 
     const int e = tid / G, h = tid % G;
     P a = M::empty();
     if (e < tile_out) {
-        a = smem[(h * per_t) * tile_out + e];
-        for (int g = 1; g < per_t; ++g) a = M::combine(a, smem[(h * per_t + g) * tile_out + e]);
+        a = smem[(h * per_t) * pitch + e];
+        for (int g = 1; g < per_t; ++g) a = M::combine(a, smem[(h * per_t + g) * pitch + e]);
     }
     for (int d = 1; d < G; d <<= 1) {
         const P o = shfl_down_width(a, d, G);

@@ -95,6 +95,8 @@ extern "C" ak_status ak_reduce_noalloc(const void* src, int64_t n, ak_dtype in, 
     // Same validation, kernels and store rules as ak_reduce; a plan needing
     // more scratch than the fixed array holds is refused there with
     // AK_ERR_WORKSPACE before anything is launched.
-    return ak_reduce(src, n, in, f, op, acc, out, init, mode, dst_dev, dst_host, scratch,
-                     (size_t)AK_NOALLOC_SCRATCH_BYTES, opts, stream);
+    // A host result is copied out of the fixed array (no pinned host slot:
+    // that would be an allocation).
+    return ak::reduce_entry(src, nullptr, 0, n, in, f, op, acc, out, init, mode, dst_dev, dst_host, scratch,
+                            (size_t)AK_NOALLOC_SCRATCH_BYTES, opts, stream, false);
 }

@@ -14,7 +14,8 @@ ak_status run_scan_i64(const ScanCall& c, const ScanPlan& p);
 ak_status run_scan_mat2(const ScanCall& c, const ScanPlan& p);
 
 ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_dtype acc, ak_dtype out, ak_op op,
-                    bool no_neutral, int target_blocks, int items, const DeviceInfo& dev, ScanPlan* p) {
+                    bool no_neutral, int target_blocks, int items, const DeviceInfo& dev, ScanPlan* p,
+                    bool single_pass) {
     (void)op;
     (void)target_blocks;
     (void)dev;
@@ -24,7 +25,7 @@ ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_d
     // the TMA tile scan takes one element type throughout: f32 / i32 / i64
     // with a neutral element (see scan::plan_sizes)
     const bool tma_type = in == acc && out == acc && (acc == AK_F32 || acc == AK_I32 || acc == AK_I64) && !no_neutral;
-    return scan::plan_sizes(inner, len, outer, asz, psz, tma_type, items, p);
+    return scan::plan_sizes(inner, len, outer, asz, psz, tma_type, items, p, ak_dtype_size(in), single_pass);
 }
 
 ak_status run_scan(const ScanCall& c, const ScanPlan& plan) {

@@ -824,6 +824,114 @@ __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Ac
 }
 
 // ---------------------------------------------------------------------------
+// Reduce-then-scan in three launches, for single lines that fit L2
+// ---------------------------------------------------------------------------
+//
+// A line whose input fits comfortably in the 129 MB L2 is too short for the
+// single-pass super-tile scan to amortise its block-wide steps (a 40 MB line
+// is under three super-tiles per block). Three launches chained with
+// programmatic dependent launch do it without any wait between blocks:
+//   fold   block t folds super-tile t: its segment totals and its aggregate
+//          go to the workspace, the tile is kept in L2 (evict_last);
+//   tiles  one block scans the aggregates into each tile's exclusive prefix
+//          (init at the front);
+//   apply  block t scans its segment totals from its prefix and every thread
+//          walks its segment again, now from L2, storing as it goes.
+// HBM traffic stays one read and one write of every element (the second
+// read hits L2), and the operator is applied twice per element.
+
+constexpr int kTilesBlock = 1024;  // threads of the one-block tile-prefix scan
+
+template <class In, class M, int BLOCK, int SEG>
+__global__ void __launch_bounds__(BLOCK) k_scan3_fold(const In* __restrict__ x, int64_t len,
+                                                      typename M::P* __restrict__ seg_out,
+                                                      typename M::P* __restrict__ agg_out, uint64_t* error_word) {
+    using P = typename M::P;
+    constexpr int W = BLOCK / kWarp;
+    constexpr int64_t SUPER = (int64_t)BLOCK * SEG;
+    __shared__ P red[W];
+    const int64_t t = blockIdx.x;
+    const int tid = threadIdx.x;
+    if (t == 0 && tid == 0) *error_word = 0;  // no waits in this scan: the call's status is ok
+    const int64_t start = t * SUPER + (int64_t)tid * SEG;
+    const int n = (int)max((int64_t)0, min((int64_t)SEG, len - start));
+    const P tot = n > 0 ? segment_fold<In, M, SEG>(x + start, n, l2_policy_evict_last()) : M::empty();
+    seg_out[t * BLOCK + tid] = tot;
+    griddep_launch_dependents();
+    const P agg = block_reduce_ordered<M, BLOCK>(tot, red);
+    if (tid == 0) agg_out[t] = agg;
+}
+
+// One block: pre[t] = init (or empty) combined with agg[0 .. t-1]. Thread r
+// folds a contiguous run of tiles, the runs are scanned across the block in
+// order, then every thread writes its tiles' prefixes.
+template <class M>
+__global__ void __launch_bounds__(kTilesBlock) k_scan3_tiles(const typename M::P* __restrict__ agg,
+                                                             typename M::P* __restrict__ pre, int64_t ntiles,
+                                                             bool has_init, typename M::acc init) {
+    using P = typename M::P;
+    constexpr int W = kTilesBlock / kWarp;
+    __shared__ P wt[W];
+    griddep_wait();
+    const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    const int64_t per = (ntiles + kTilesBlock - 1) / kTilesBlock;
+    const int64_t t0 = min(ntiles, (int64_t)tid * per), t1 = min(ntiles, t0 + per);
+    P run = M::empty();
+    for (int64_t t = t0; t < t1; ++t) run = M::combine(run, agg[t]);
+    const P inc = warp_inclusive_scan<M>(run, lane);
+    P lane_excl = shfl_up_any(inc, 1);
+    if (lane == 0) lane_excl = M::empty();
+    if (lane == kWarp - 1) wt[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const P w = lane < W ? wt[lane] : M::empty();
+        const P wi = warp_inclusive_scan<M>(w, lane);
+        P we = shfl_up_any(wi, 1);
+        if (lane == 0) we = M::empty();
+        wt[lane] = we;
+    }
+    __syncthreads();
+    griddep_launch_dependents();
+    P a = M::combine(M::combine(has_init ? M::lift(init) : M::empty(), wt[warp]), lane_excl);
+    for (int64_t t = t0; t < t1; ++t) {
+        pre[t] = a;
+        a = M::combine(a, agg[t]);
+    }
+}
+
+template <class In, class Acc, class Out, class M, int BLOCK, int SEG>
+__global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Acc)>())
+    k_scan3_apply(const In* __restrict__ x, Out* __restrict__ y, int64_t len,
+                  const typename M::P* __restrict__ seg_tot, const typename M::P* __restrict__ pre, bool excl) {
+    using P = typename M::P;
+    constexpr int W = BLOCK / kWarp;
+    constexpr int64_t SUPER = (int64_t)BLOCK * SEG;
+    __shared__ P warp_tot[W];
+    griddep_wait();
+    const int64_t t = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    const P tot = seg_tot[t * BLOCK + tid];
+    const P inc = warp_inclusive_scan<M>(tot, lane);
+    P lane_excl = shfl_up_any(inc, 1);
+    if (lane == 0) lane_excl = M::empty();
+    if (lane == kWarp - 1) warp_tot[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const P w = lane < W ? warp_tot[lane] : M::empty();
+        const P wi = warp_inclusive_scan<M>(w, lane);
+        P we = shfl_up_any(wi, 1);
+        if (lane == 0) we = M::empty();
+        if (lane < W) warp_tot[lane] = we;
+    }
+    __syncthreads();
+    const P mine = M::combine(M::combine(pre[t], warp_tot[warp]), lane_excl);
+    const int64_t start = t * SUPER + (int64_t)tid * SEG;
+    const int n = (int)max((int64_t)0, min((int64_t)SEG, len - start));
+    const uint64_t last_use = l2_policy_evict_first();
+    if (n > 0) segment_scan_store<In, Out, M, SEG>(x + start, y + start, n, mine, last_use, last_use, excl);
+}
+
+// ---------------------------------------------------------------------------
 // TMA tile scan: one read and one write of every element
 // ---------------------------------------------------------------------------
 
@@ -1503,6 +1611,33 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
             if (c.len <= 64 * ITEMS) lines(std::integral_constant<int, 64>{});
             else if (c.len <= 128 * ITEMS || BLOCK == 128) lines(std::integral_constant<int, 128>{});
             else lines(std::integral_constant<int, BLOCK>{});
+        } else if (p.three) {
+            // reduce-then-scan: fold, tile prefixes, apply (PDL-chained)
+            P* seg = reinterpret_cast<P*>(ws + p.seg_off);
+            P* agg = reinterpret_cast<P*>(ws + p.agg_off);
+            P* pre = reinterpret_cast<P*>(ws + p.pre_off);
+            k_scan3_fold<In, M, BLOCK, SEG><<<(unsigned)p.tiles, BLOCK, 0, c.stream>>>(
+                static_cast<const In*>(c.src), c.len, seg, agg, reinterpret_cast<uint64_t*>(ws));
+            ak_status s = check_launch();
+            if (s != AK_OK) return s;
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            cfg.stream = c.stream;
+            cfg.gridDim = dim3(1);
+            cfg.blockDim = dim3(kTilesBlock);
+            cudaError_t e = cudaLaunchKernelEx(&cfg, k_scan3_tiles<M>, (const P*)agg, pre, p.tiles, c.has_init, init);
+            if (e != cudaSuccess) return cuda_fail(e);
+            cfg.gridDim = dim3((unsigned)p.tiles);
+            cfg.blockDim = dim3(BLOCK);
+            e = cudaLaunchKernelEx(&cfg, k_scan3_apply<In, Acc, Out, M, BLOCK, SEG>, static_cast<const In*>(c.src),
+                                   static_cast<Out*>(c.dst), c.len, (const P*)seg, (const P*)pre, c.exclusive);
+            if (e != cudaSuccess) return cuda_fail(e);
+            count_launches(3);
+            return AK_OK;
         } else {
             DeviceInfo dev;
             if (!current_device(&dev)) return AK_ERR_CUDA;
@@ -1536,8 +1671,14 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
 // combine; those run faster as super-tiles, whose blocks carry more warps per
 // SM); it then also needs rows of 128 bytes, several tiles per line, and
 // lines that start on a row boundary unless there is only one.
+// The largest line input taken by the three-launch reduce-then-scan: well
+// inside the 129 MB L2, so its second read hits.
+constexpr uint64_t kThreePassMaxBytes = 64ull << 20;
+
 inline ak_status plan_sizes(int64_t inner, int64_t len, int64_t outer, size_t asz, size_t psz, bool tma_type,
-                            int items, ScanPlan* p) {
+                            int items, ScanPlan* p, size_t in_bytes = 0, bool single_pass = false) {
+    p->three = false;
+    p->seg_off = p->agg_off = p->pre_off = 0;
     p->state_off = kWsHeader;
     p->ws_bytes = kWsHeader;
     p->tiles = 0;
@@ -1580,6 +1721,18 @@ inline ak_status plan_sizes(int64_t inner, int64_t len, int64_t outer, size_t as
         p->tma_tiles = p->tma_tiles_per_line * outer;
         p->tma_ws_bytes = align_up(kWsHeader + (size_t)p->tma_tiles * (16 + align_up(psz, 16)), 256);
         p->ws_bytes = std::max(p->ws_bytes, p->tma_ws_bytes);
+    }
+    // one line whose input fits well inside L2, outside the TMA scan:
+    // reduce-then-scan in three launches (in_bytes = 0: unknown, not taken;
+    // single_pass: the caller wants the single-pass kernel, e.g. to exercise
+    // its bounded waits)
+    const uint64_t in_total = (uint64_t)in_bytes * (uint64_t)len;
+    if (!p->tma && outer == 1 && in_bytes != 0 && !single_pass && in_total <= kThreePassMaxBytes) {
+        p->three = true;
+        p->seg_off = kWsHeader;
+        p->agg_off = align_up(p->seg_off + (size_t)p->tiles * block * psz, 256);
+        p->pre_off = align_up(p->agg_off + (size_t)p->tiles * psz, 256);
+        p->ws_bytes = std::max(p->ws_bytes, align_up(p->pre_off + (size_t)p->tiles * psz, 256));
     }
     return AK_OK;
 }

@@ -121,12 +121,12 @@ def test_accumulate_validates_and_plans_on_host(L):
 def test_dims_selector(L):
     import mapreduce_prefix_scan_gb300 as ak
     # 3072 x 2048 bf16, dims=2 (12.6 MB, latency-bound): 16-byte vectors of 8,
-    # 8 threads across a 64-output row segment, 32 row groups of 4 rows, the
+    # 16 threads across a 128-output row segment, 16 row groups of 8 rows, the
     # reduction split 16 ways and the split blocks of an output tile combined
-    # in a thread-block cluster: 768 blocks of 16 KB
+    # in a thread-block cluster: 384 blocks of 32 KB, all resident at once
     shape, tile, groups, split = ak.ak_dims_select(3072, 2048, 1, 2, 8, 152)
-    assert shape == "columns" and tile == 64 and groups == 32 and split == 16
-    assert (3072 // tile) * split == 768 and 2048 // (split * groups) == 4
+    assert shape == "columns" and tile == 128 and groups == 16 and split == 16
+    assert (3072 // tile) * split == 384 and 2048 // (split * groups) == 8
     # a larger input: a warp across a 256-output row segment, 8 row groups,
     # split through the workspace and a second pass, >= 1 block per SM
     shape, tile, groups, split = ak.ak_dims_select(3072, 8192, 1, 2, 8, 152)
