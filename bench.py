@@ -629,6 +629,16 @@ def run_profile(case: str):
         idx = torch.empty(10**8, dtype=torch.int64, device=dev)
         cnt = torch.empty(1, dtype=torch.int64, device=dev)
         fn = lambda: ak.ak_findall(x, idx=idx, count=cnt, to_host=False)
+    elif case == "findall_small":  # 2e7 Bool flags, half set (200 MB of indices out)
+        w = synth.words(2 * 10**7, 0, 90)
+        x = torch.from_numpy(((w >> np.uint64(63)) == 1).astype(np.uint8)).to(dev)
+        idx = torch.empty(2 * 10**7, dtype=torch.int64, device=dev)
+        cnt = torch.empty(1, dtype=torch.int64, device=dev)
+        fn = lambda: ak.ak_findall(x, idx=idx, count=cnt, to_host=False)
+    elif case == "dims_rows":  # 4096 x 4096 f32, sum(x; dims=1): contiguous reductions
+        x = torch.from_numpy(synth.normal_f32(4096 * 4096, 0, 41)).reshape(4096, 4096).to(dev)
+        d1 = torch.empty(4096, dtype=torch.float32, device=dev)
+        fn = lambda: ak.ak_reduce_dims(x, [0], dst=d1)
     elif case == "dims_big":  # 8192 x 8192 f32, sum(x; dims=2)
         x = torch.from_numpy(synth.normal_f32(8192 * 8192, 0, 40)).reshape(8192, 8192).to(dev)
         fn = lambda: ak.ak_reduce_dims(x, [1])
@@ -651,7 +661,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--small", action="store_true", help="n = 1e6 (quick runs)")
     ap.add_argument("--profile", default=None, help="run a small ncu case: reduce|scan|scan_f32|scan_max|scan_mat2|"
-                    "scan_lines|scan_lines_mat2|findall|dims|dims_big")
+                    "scan_lines|scan_lines_mat2|findall|findall_small|dims|dims_rows|dims_big")
     args = ap.parse_args()
     if args.profile:
         run_profile(args.profile)

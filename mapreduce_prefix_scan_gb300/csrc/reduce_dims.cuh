@@ -245,7 +245,43 @@ __global__ void __launch_bounds__(kBlock) k_dims_rows(const In* __restrict__ x, 
     const int64_t js = (int64_t)s * jper, je = min(J, js + jper);
     const In* row = x + ldk * k;
     P a = M::empty();
-    if constexpr (M::commutative) {
+    if constexpr (M::commutative && sizeof(In) < 16 && 16 % sizeof(In) == 0) {
+        // 16-byte vector loads, U per lane at a time: an element-wise
+        // head up to the first 16-byte boundary, the vectors, an element-wise tail
+        constexpr int V = 16 / (int)sizeof(In);
+        constexpr int U = 4;
+        const In* seg = row + js;
+        const int64_t len = je - js;
+        const int64_t head = min(len, (int64_t)(((16 - reinterpret_cast<uintptr_t>(seg) % 16) % 16) / sizeof(In)));
+        const int64_t nvec = (len - head) / V;
+        P acc[V];
+#pragma unroll
+        for (int q = 0; q < V; ++q) acc[q] = M::empty();
+        for (int64_t i = lane; i < head; i += kWarp) acc[0] = M::combine(acc[0], lift_elem<In, Acc, Map, M>(seg[i]));
+        const In* body = seg + head;
+        int64_t v = lane;
+        for (; v + (U - 1) * kWarp < nvec; v += U * kWarp) {
+            Raw<16> r[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) r[u] = ld_stream16(body + (v + u * kWarp) * V);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int q = 0; q < V; ++q)
+                    acc[q] = M::combine(acc[q], lift_elem<In, Acc, Map, M>(raw_get<In>(r[u], q)));
+        }
+        for (; v < nvec; v += kWarp) {
+            const Raw<16> r = ld_stream16(body + v * V);
+#pragma unroll
+            for (int q = 0; q < V; ++q) acc[q] = M::combine(acc[q], lift_elem<In, Acc, Map, M>(raw_get<In>(r, q)));
+        }
+        for (int64_t i = head + nvec * V + lane; i < len; i += kWarp)
+            acc[V - 1] = M::combine(acc[V - 1], lift_elem<In, Acc, Map, M>(seg[i]));
+        a = acc[0];
+#pragma unroll
+        for (int q = 1; q < V; ++q) a = M::combine(a, acc[q]);
+        a = warp_reduce<M>(a);
+    } else if constexpr (M::commutative) {
         int64_t j = js + lane;
         for (; j + 3 * kWarp < je; j += 4 * kWarp) {
             In v0 = row[j], v1 = row[j + kWarp], v2 = row[j + 2 * kWarp], v3 = row[j + 3 * kWarp];
