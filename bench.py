@@ -174,17 +174,25 @@ def _time_call(fn, reps, flush_buf, torch, host_sync=False):
     start event, so the call's host work (argument marshalling, the plan)
     is done and its kernels are queued by the time the event fires. A call
     that synchronizes on the host (host_sync: a host result) cannot be
-    queued ahead; it is timed as the user sees it, host work included."""
+    queued ahead; it is timed by the host clock, as the caller sees it."""
     s = torch.cuda.current_stream()
     ts = []
     for _ in range(3):
         fn()
     for _ in range(reps):
         _flush_l2(flush_buf)
+        if host_sync:
+            # the call returns only once its result is on the host: its wall
+            # time is what the caller sees (host work, launches, the
+            # synchronisation and the host finish)
+            torch.cuda.synchronize()
+            t = time.perf_counter()
+            fn()
+            ts.append((time.perf_counter() - t) * 1e6)
+            continue
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        if not host_sync:
-            torch.cuda._sleep(200_000)
+        torch.cuda._sleep(200_000)
         e0.record(s)
         fn()
         e1.record(s)
