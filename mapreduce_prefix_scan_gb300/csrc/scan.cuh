@@ -824,23 +824,28 @@ __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Ac
 }
 
 // ---------------------------------------------------------------------------
-// Reduce-then-scan in three launches, for single lines that fit L2
+// Reduce-then-scan in three launches, for single long lines
 // ---------------------------------------------------------------------------
 //
-// A line whose input fits comfortably in the 129 MB L2 is too short for the
-// single-pass super-tile scan to amortise its block-wide steps (a 40 MB line
-// is under three super-tiles per block). Three launches chained with
-// programmatic dependent launch do it without any wait between blocks:
+// A single long line outside the TMA scan (f64, matrices, Optional
+// partials, mixed types) is scanned by three launches chained with
+// programmatic dependent launch, without any wait between blocks:
 //   fold   block t folds super-tile t: its segment totals and its aggregate
 //          go to the workspace, the tile is kept in L2 (evict_last);
 //   tiles  one block scans the aggregates into each tile's exclusive prefix
-//          (init at the front);
+//          (init at the front) -- or, for up to kFusedPrefixTiles tiles, each
+//          apply block folds the aggregates before it itself;
 //   apply  block t scans its segment totals from its prefix and every thread
-//          walks its segment again, now from L2, storing as it goes.
-// HBM traffic stays one read and one write of every element (the second
-// read hits L2), and the operator is applied twice per element.
+//          walks its segment again, storing as it goes.
+// A line that fits L2 is read from HBM once (the second read hits); a longer
+// one pays part of the second read, but on GB300 the single-pass super-tile
+// scan, whose blocks wait on each other's look-backs, is slower at every
+// length measured. The operator is applied twice per element either way.
 
 constexpr int kTilesBlock = 1024;  // threads of the one-block tile-prefix scan
+// Up to this many tiles the apply blocks fold the aggregates before them
+// themselves (at most this many reads per block, from L2).
+constexpr int64_t kFusedPrefixTiles = 256;
 
 template <class In, class M, int BLOCK, int SEG>
 __global__ void __launch_bounds__(BLOCK) k_scan3_fold(const In* __restrict__ x, int64_t len,
@@ -899,17 +904,34 @@ __global__ void __launch_bounds__(kTilesBlock) k_scan3_tiles(const typename M::P
     }
 }
 
+// Block t scans tile t. Its exclusive prefix comes from k_scan3_tiles
+// (pre != nullptr), or (pre == nullptr) the block folds it itself: init (or
+// the neutral element) combined with the aggregates of tiles 0 .. t-1, the
+// threads taking consecutive runs that are combined in order.
 template <class In, class Acc, class Out, class M, int BLOCK, int SEG>
 __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Acc)>())
     k_scan3_apply(const In* __restrict__ x, Out* __restrict__ y, int64_t len,
-                  const typename M::P* __restrict__ seg_tot, const typename M::P* __restrict__ pre, bool excl) {
+                  const typename M::P* __restrict__ seg_tot, const typename M::P* __restrict__ pre,
+                  const typename M::P* __restrict__ agg, bool has_init, Acc init, bool excl) {
     using P = typename M::P;
     constexpr int W = BLOCK / kWarp;
     constexpr int64_t SUPER = (int64_t)BLOCK * SEG;
     __shared__ P warp_tot[W];
+    __shared__ P red[W];
+    __shared__ P s_pre;
     griddep_wait();
     const int64_t t = blockIdx.x;
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    if (pre == nullptr) {
+        const int64_t per = (t + BLOCK - 1) / BLOCK;
+        const int64_t a0 = min(t, (int64_t)tid * per), a1 = min(t, a0 + per);
+        P f = M::empty();
+        for (int64_t q = a0; q < a1; ++q) f = M::combine(f, agg[q]);
+        f = block_reduce_ordered<M, BLOCK>(f, red);
+        if (tid == 0) s_pre = M::combine(has_init ? M::lift(init) : M::empty(), f);
+        __syncthreads();
+    }
+    const P tile_pre = pre == nullptr ? s_pre : pre[t];
     const P tot = seg_tot[t * BLOCK + tid];
     const P inc = warp_inclusive_scan<M>(tot, lane);
     P lane_excl = shfl_up_any(inc, 1);
@@ -924,7 +946,7 @@ __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Ac
         if (lane < W) warp_tot[lane] = we;
     }
     __syncthreads();
-    const P mine = M::combine(M::combine(pre[t], warp_tot[warp]), lane_excl);
+    const P mine = M::combine(M::combine(tile_pre, warp_tot[warp]), lane_excl);
     const int64_t start = t * SUPER + (int64_t)tid * SEG;
     const int n = (int)max((int64_t)0, min((int64_t)SEG, len - start));
     const uint64_t last_use = l2_policy_evict_first();
@@ -1616,10 +1638,6 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
             P* seg = reinterpret_cast<P*>(ws + p.seg_off);
             P* agg = reinterpret_cast<P*>(ws + p.agg_off);
             P* pre = reinterpret_cast<P*>(ws + p.pre_off);
-            k_scan3_fold<In, M, BLOCK, SEG><<<(unsigned)p.tiles, BLOCK, 0, c.stream>>>(
-                static_cast<const In*>(c.src), c.len, seg, agg, reinterpret_cast<uint64_t*>(ws));
-            ak_status s = check_launch();
-            if (s != AK_OK) return s;
             cudaLaunchConfig_t cfg = {};
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1627,16 +1645,29 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             cfg.stream = c.stream;
-            cfg.gridDim = dim3(1);
-            cfg.blockDim = dim3(kTilesBlock);
-            cudaError_t e = cudaLaunchKernelEx(&cfg, k_scan3_tiles<M>, (const P*)agg, pre, p.tiles, c.has_init, init);
-            if (e != cudaSuccess) return cuda_fail(e);
+            const In* xs = static_cast<const In*>(c.src);
+            Out* ys = static_cast<Out*>(c.dst);
+            uint64_t* err = reinterpret_cast<uint64_t*>(ws);
+            k_scan3_fold<In, M, BLOCK, SEG><<<(unsigned)p.tiles, BLOCK, 0, c.stream>>>(xs, c.len, seg, agg, err);
+            ak_status s = check_launch();
+            if (s != AK_OK) return s;
+            // few tiles: the apply blocks fold the aggregates before them
+            // themselves; many: one block scans them first
+            const bool fused = p.tiles <= kFusedPrefixTiles;
+            if (!fused) {
+                cfg.gridDim = dim3(1);
+                cfg.blockDim = dim3(kTilesBlock);
+                const cudaError_t e =
+                    cudaLaunchKernelEx(&cfg, k_scan3_tiles<M>, (const P*)agg, pre, p.tiles, c.has_init, init);
+                if (e != cudaSuccess) return cuda_fail(e);
+            }
             cfg.gridDim = dim3((unsigned)p.tiles);
             cfg.blockDim = dim3(BLOCK);
-            e = cudaLaunchKernelEx(&cfg, k_scan3_apply<In, Acc, Out, M, BLOCK, SEG>, static_cast<const In*>(c.src),
-                                   static_cast<Out*>(c.dst), c.len, (const P*)seg, (const P*)pre, c.exclusive);
+            const cudaError_t e = cudaLaunchKernelEx(
+                &cfg, k_scan3_apply<In, Acc, Out, M, BLOCK, SEG>, xs, ys, c.len, (const P*)seg,
+                fused ? (const P*)nullptr : (const P*)pre, (const P*)agg, c.has_init, init, c.exclusive);
             if (e != cudaSuccess) return cuda_fail(e);
-            count_launches(3);
+            count_launches(fused ? 2 : 3);
             return AK_OK;
         } else {
             DeviceInfo dev;
@@ -1671,9 +1702,12 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
 // combine; those run faster as super-tiles, whose blocks carry more warps per
 // SM); it then also needs rows of 128 bytes, several tiles per line, and
 // lines that start on a row boundary unless there is only one.
-// The largest line input taken by the three-launch reduce-then-scan: well
-// inside the 129 MB L2, so its second read hits.
-constexpr uint64_t kThreePassMaxBytes = 64ull << 20;
+// Single lines not on the TMA scan take the reduce-then-scan in three
+// launches at any length: on GB300 it beat the single-pass super-tile scan
+// at every size measured, even where the second read misses L2 (1e8 f64:
+// 418 against 444 us; 1e8 f32 max under Optional partials: 231 against 332
+// us; 1e7 mod-p products: level), because no block ever waits on another.
+constexpr uint64_t kThreePassMaxBytes = ~0ull;
 
 inline ak_status plan_sizes(int64_t inner, int64_t len, int64_t outer, size_t asz, size_t psz, bool tma_type,
                             int items, ScanPlan* p, size_t in_bytes = 0, bool single_pass = false) {
@@ -1722,10 +1756,9 @@ inline ak_status plan_sizes(int64_t inner, int64_t len, int64_t outer, size_t as
         p->tma_ws_bytes = align_up(kWsHeader + (size_t)p->tma_tiles * (16 + align_up(psz, 16)), 256);
         p->ws_bytes = std::max(p->ws_bytes, p->tma_ws_bytes);
     }
-    // one line whose input fits well inside L2, outside the TMA scan:
-    // reduce-then-scan in three launches (in_bytes = 0: unknown, not taken;
-    // single_pass: the caller wants the single-pass kernel, e.g. to exercise
-    // its bounded waits)
+    // one line outside the TMA scan: reduce-then-scan in three launches
+    // (in_bytes = 0: unknown, not taken; single_pass: the caller wants the
+    // single-pass kernel, e.g. to exercise its bounded waits)
     const uint64_t in_total = (uint64_t)in_bytes * (uint64_t)len;
     if (!p->tma && outer == 1 && in_bytes != 0 && !single_pass && in_total <= kThreePassMaxBytes) {
         p->three = true;

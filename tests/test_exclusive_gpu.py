@@ -156,3 +156,26 @@ def test_scan_status_reports_ok_and_a_silent_timeout():
     ak.ak_accumulate(m, dim=0, workspace=ws)
     torch.cuda.synchronize()
     assert ak.ak_scan_status(ws) == 0
+
+
+@pytest.mark.parametrize("exclusive", [False, True])
+def test_long_single_lines_with_init(exclusive):
+    # single lines outside the TMA scan, long enough that the tile prefixes
+    # come from the one-block prefix scan rather than from each apply block
+    n = 5 * 10**6 + 17                          # 40 MB of f64
+    x = synth.uniform_f64_01(n, stream=90)
+    y = ak.ak_accumulate(dev_of("f64", x), init=0.5, exclusive=exclusive).cpu().numpy()
+    want = oracle.scan(x, "f64", init=0.5, exclusive=exclusive)
+    mass = (_excl_mass(x, (n,), -1, 0.5) if exclusive else np.cumsum(x) + 0.5)
+    assert_close_f32(y, want, mass, rel=F64_REL)
+    m = 3 * 10**6 + 5                           # 48 MB of 2x2 matrices mod p
+    xm = synth.mat2_modp(m, stream=91)
+    init = synth.mat2_modp(1, stream=92)[0]
+    ym = ak.ak_accumulate(dev_of("mat2", xm), op="matmul", elem="mat2", init=init, exclusive=exclusive)
+    assert_exact(ym.cpu().numpy().view(np.uint32).reshape(-1, 4),
+                 oracle.scan(xm, "mat2", init=init, exclusive=exclusive))
+    k = 2 * 10**7 + 3                           # 80 MB of f32 under Optional partials
+    xo = synth.normal_f32(k, stream=93)
+    yo = ak.ak_accumulate(dev_of("f32", xo), op="max", init=-0.25, exclusive=exclusive,
+                          opts=ak.make_opts(no_neutral=True, exclusive=exclusive)).cpu().numpy()
+    assert_exact(yo.astype(np.float64), oracle.scan(xo, "f32", op="max", init=-0.25, exclusive=exclusive))
