@@ -16,15 +16,16 @@ ak_status run_scan_mat2(const ScanCall& c, const ScanPlan& p);
 ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_dtype acc, ak_dtype out, ak_op op,
                     bool no_neutral, int target_blocks, int items, const DeviceInfo& dev, ScanPlan* p,
                     bool single_pass) {
-    (void)op;
     (void)target_blocks;
     (void)dev;
     const size_t psz = partial_size(acc, no_neutral);
     const size_t asz = ak_dtype_size(acc);
     if (!psz || !asz) return AK_ERR_UNSUPPORTED;
     // the TMA tile scan takes one element type throughout: f32 / i32 / i64
-    // with a neutral element (see scan::plan_sizes)
-    const bool tma_type = in == acc && out == acc && (acc == AK_F32 || acc == AK_I32 || acc == AK_I64) && !no_neutral;
+    // with a neutral element, and f64 sums (whose row folds run in fixed
+    // point, so that only the scan itself uses the FP64 pipe)
+    const bool tma_type = in == acc && out == acc && !no_neutral &&
+                          (acc == AK_F32 || acc == AK_I32 || acc == AK_I64 || (acc == AK_F64 && op == AK_OP_ADD));
     return scan::plan_sizes(inner, len, outer, asz, psz, tma_type, items, p, ak_dtype_size(in), single_pass);
 }
 

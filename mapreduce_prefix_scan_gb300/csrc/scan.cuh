@@ -2,16 +2,20 @@
 // the kernels and their launchers, as templates (compiled into libak for the
 // built-in operators and into a caller's translation unit by include/ak.hpp).
 //
-// Four kernels, chosen per call:
+// The kernels, chosen per call:
 //
 //  * k_scan_tma -- long contiguous lines of f32 / i32 / i64 with a neutral
-//    element: one persistent block per SM runs a ring of 32 KB tiles copied
-//    by the TMA engine through producer, fold, look-back and scan warps
-//    (described at the kernel). Every element is read once and written once.
-//  * k_scan_tiles -- other long contiguous lines (f64, the matrix product,
-//    Optional partials, mixed input and accumulator types): persistent
-//    blocks claim super-tiles, fold them (phase A) and scan them one round
-//    later from L2 (phase B).
+//    element, and f64 sums: one persistent block per SM runs a ring of 32 KB
+//    tiles copied by the TMA engine through producer, fold, look-back and
+//    scan warps (described at the kernel). Every element is read once and
+//    written once.
+//  * k_scan3_fold / k_scan3_tiles / k_scan3_apply -- other single long
+//    lines (f64 max / min / products, the matrix product, Optional
+//    partials, mixed input and accumulator types): reduce-then-scan in
+//    three launches, no block waiting on another.
+//  * k_scan_tiles -- several such lines: persistent blocks claim
+//    super-tiles, fold them (phase A) and scan them one round later from L2
+//    (phase B).
 //  * k_scan_lines -- lines that fit one tile (e.g. dims=1 of a matrix):
 //    one block per line, no state shared between blocks.
 //  * k_scan_strided -- lines along a strided dimension: a thread per column.
@@ -589,6 +593,105 @@ __device__ __forceinline__ double row_sum_fixed(const double (&run)[R]) {
     return scalbn((double)sum, (int)emax - 1081);
 }
 
+// Wide fixed point for f64 sums on the integer pipes (GB300 runs FP64 at a
+// small fraction of its integer rate, so the TMA scan of f64 sums keeps
+// FP64 off the per-element path). A partial is (a, e): the value
+// a * 2^(e - kFxK), a a signed 64-bit integer, e >= 1 a biased binary
+// exponent. A finite double enters exactly, at its own exponent with kFxG
+// guard bits; two partials add at the larger exponent (the other one's bits
+// below it are truncated, an error under one unit there); a partial is
+// renormalised to at most L significant bits before headroom runs out. Every
+// truncation is below 2^-53 of a magnitude that the sum of |x| over the
+// elements involved bounds, far inside the f64 scan tolerance.
+struct Fx {
+    int64_t a;
+    int32_t e;
+    int32_t pad;
+};
+constexpr int kFxG = 3;
+constexpr int kFxK = 1075 + kFxG;
+constexpr uint64_t kF64Frac = 0x000FFFFFFFFFFFFFull;
+constexpr uint64_t kF64NegZero = 0x8000000000000000ull;
+
+__device__ __forceinline__ Fx fx_zero() { return Fx{0, 1, 0}; }
+
+// a >> d for d >= 0 (arithmetic; d >= 64 leaves the sign)
+__device__ __forceinline__ int64_t fx_shr(int64_t a, int d) { return a >> min(d, 63); }
+
+__device__ __forceinline__ Fx fx_add(const Fx& x, const Fx& y) {
+    const int e = max(x.e, y.e);
+    return Fx{fx_shr(x.a, e - x.e) + fx_shr(y.a, e - y.e), e, 0};
+}
+
+// |a| < 2^L afterwards
+__device__ __forceinline__ Fx fx_norm(Fx x, int L) {
+    const uint64_t m = (uint64_t)(x.a < 0 ? -x.a : x.a);
+    const int s = max(0, 64 - __clzll((long long)m) - L);
+    x.a >>= s;
+    x.e += s;
+    return x;
+}
+
+// A finite double, exactly (|a| < 2^56).
+__device__ __forceinline__ Fx fx_of(double v) {
+    const uint64_t b = (uint64_t)__double_as_longlong(v);
+    const int f = (int)((b >> 52) & 0x7FFu);
+    const int64_t m = (int64_t)(((b & kF64Frac) | (f != 0 ? 1ull << 52 : 0ull)) << kFxG);
+    return Fx{(b >> 63) ? -m : m, max(f, 1), 0};
+}
+
+// Rounded to the nearest double (ties away from zero); zero gives +0. A
+// result below the normal range or above the largest double takes the
+// library scaling (rare).
+__device__ __forceinline__ double fx_to_double(const Fx& x) {
+    if (x.a == 0) return 0.0;
+    const uint64_t mag = (uint64_t)(x.a < 0 ? -x.a : x.a);
+    const int lz = __clzll((long long)mag);
+    const uint64_t nm = mag << lz;  // leading one at bit 63
+    // nm >> 11 is the 53-bit significand, the value nm * 2^(e - kFxK - lz)
+    const int B = x.e - kFxG - lz + 11;
+    if (B < 1 || B > 2046) return scalbn((double)x.a, x.e - kFxK);
+    // a carry out of the significand moves into the exponent field
+    const uint64_t bits = ((uint64_t)(B - 1) << 52) + (nm >> 11) + ((nm >> 10) & 1u);
+    return __longlong_as_double((long long)(bits | (x.a < 0 ? kF64NegZero : 0ull)));
+}
+
+__device__ __forceinline__ Fx fx_shfl_up(const Fx& v, int d) {
+    return Fx{(int64_t)__shfl_up_sync(0xffffffffu, (long long)v.a, d), __shfl_up_sync(0xffffffffu, v.e, d), 0};
+}
+__device__ __forceinline__ Fx fx_shfl_idx(const Fx& v, int lane) {
+    return Fx{(int64_t)__shfl_sync(0xffffffffu, (long long)v.a, lane), __shfl_sync(0xffffffffu, v.e, lane), 0};
+}
+
+// Sum of a row of doubles at the row's largest exponent: the 53-bit
+// significands are aligned there without guard bits (each truncation is
+// under one unit in the last place of the row's largest element) and the
+// guard scale goes into the exponent (|a| < 2^57). *fmax is the largest
+// exponent field: 0x7FF when the row holds an infinity or a NaN, 0 when it
+// holds only zeros and subnormals (the caller then takes the FP64 path,
+// which keeps IEEE specials and signed zeros).
+template <int R>
+__device__ __forceinline__ Fx row_total_fx(const double (&run)[R], int* fmax) {
+    int f[R];
+    int fm = 0;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        f[i] = (int)(((uint32_t)__double2hiint(run[i]) >> 20) & 0x7FFu);
+        fm = max(fm, f[i]);
+    }
+    const int emax = max(fm, 1);
+    int64_t sum = 0;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const uint64_t b = (uint64_t)__double_as_longlong(run[i]);
+        const uint64_t m = (b & kF64Frac) | (f[i] != 0 ? 1ull << 52 : 0ull);
+        const int64_t q = (int64_t)(m >> min(emax - max(f[i], 1), 63));
+        sum += (b >> 63) ? -q : q;
+    }
+    *fmax = fm;
+    return Fx{sum, emax + kFxG, 0};
+}
+
 // Fold of one segment (n <= SEG valid elements) in element order.
 template <class In, class M, int SEG>
 __device__ __forceinline__ typename M::P segment_fold(const In* src, int n, uint64_t policy) {
@@ -827,8 +930,9 @@ __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Ac
 // Reduce-then-scan in three launches, for single long lines
 // ---------------------------------------------------------------------------
 //
-// A single long line outside the TMA scan (f64, matrices, Optional
-// partials, mixed types) is scanned by three launches chained with
+// A single long line outside the TMA scan (matrices, Optional partials,
+// mixed types, f64 operators other than the sum) is scanned by three
+// launches chained with
 // programmatic dependent launch, without any wait between blocks:
 //   fold   block t folds super-tile t: its segment totals and its aggregate
 //          go to the workspace, the tile is kept in L2 (evict_last);
@@ -964,9 +1068,18 @@ template <class P>
 constexpr int ws_stages() {
     return sizeof(P) <= 16 ? 6 : 5;
 }
-template <class P>
+// f64 sums keep their in-tile row prefixes as wide fixed-point partials.
+template <class T, class M>
+constexpr bool ws_fx() {
+    return std::is_same_v<T, double> && std::is_same_v<typename M::op, OpAdd>;
+}
+template <class T, class M>
+constexpr int ws_rowpre_bytes() {
+    return ws_fx<T, M>() ? (int)sizeof(Fx) : (int)sizeof(typename M::P);
+}
+template <class T, class M>
 constexpr int ws_smem_bytes() {
-    return ws_stages<P>() * (kWsRows * 128 + kWsRows * (int)sizeof(P)) + 1024;
+    return ws_stages<typename M::P>() * (kWsRows * 128 + kWsRows * ws_rowpre_bytes<T, M>()) + 1024;
 }
 
 // Row r of a swizzled tile <-> the R elements of a thread, 16 bytes at a time.
@@ -1139,7 +1252,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     extern __shared__ unsigned char dyn_smem[];
     unsigned char* const bufs =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
-    P* const rowpre = reinterpret_cast<P*>(bufs + (size_t)S * TILE_BYTES);  // [S][ROWS]
+    constexpr bool FX = ws_fx<T, M>();
+    constexpr int RPB = ws_rowpre_bytes<T, M>();
+    unsigned char* const rowpre = bufs + (size_t)S * TILE_BYTES;  // [S][ROWS] slots of RPB bytes
+    auto rowpre_at = [&](int s, int r) { return rowpre + ((size_t)s * ROWS + r) * RPB; };
     __shared__ __align__(8) uint64_t full[S], folded[S], ready[S], empty[S];
     __shared__ int64_t s_k[S];
     __shared__ int64_t s_kprev[S];  // the block's tile before s_k[s] (-1: none)
@@ -1148,6 +1264,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     __shared__ P s_agg[S];
     __shared__ P s_pre[S];
     __shared__ P fwt[ROWS / 32];
+    // f64 sums: warp totals and flags of the fold, double-buffered by tile
+    // parity (no warp gets a whole tile ahead of another), and whether the
+    // tile took the FP64 path
+    __shared__ Fx fwt_fx[2][ROWS / 32];
+    __shared__ int s_wsp[2][ROWS / 32];
+    __shared__ int s_special[S];
     // hand-off between the look-back warps, in tile order: after ring slot
     // s_chain - 1, the inclusive prefix of that slot's tile is s_incl;
     // s_end is the slot of the end-of-claims sentinel once it is known
@@ -1169,7 +1291,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 #pragma unroll
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&folded[s], 1);
+            mbar_init(&folded[s], FX ? ROWS / 32 : 1);  // f64 sums: every fold warp arrives
             mbar_init(&ready[s], 1);
             mbar_init(&empty[s], ROWS / 32);
         }
@@ -1249,6 +1371,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 }
                 return;
             }
+
             // Give the other blocks time to publish the tiles they claimed
             // just before this one: wait until the next kWsLookDefer stages
             // of this block are folded too (their copies were started after
@@ -1305,14 +1428,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     for (int q = 0; q < Q; ++q)
                         if ((pend & (1u << q)) && rec_decode<P>(w[q], ctl.epoch, &vals[q]) != 0) pend &= ~(1u << q);
                 }
-                P v = M::empty();
-#pragma unroll
-                for (int q = 0; q < Q; ++q)
-                    if (mine + q < k) v = M::combine(v, vals[q]);
                 if (__any_sync(kFull, !good)) {
                     good = false;
                     break;
                 }
+                P v = M::empty();
+#pragma unroll
+                for (int q = 0; q < Q; ++q)
+                    if (mine + q < k) v = M::combine(v, vals[q]);
                 v = warp_reduce<M>(v);  // lane 0 holds the ordered fold of the batch
                 f = M::combine(f, shfl_idx_any(v, 0));
             }
@@ -1324,6 +1447,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             {
                 const uint64_t t0 = globaltimer_ns();
                 for (int i = 0; s_chain != j; ++i) {
+                    __nanosleep(64);  // leave the issue slots to the other roles
                     if (globaltimer_ns() - t0 > (uint64_t)ctl.wait_limit_ns || ((i & 63) == 63 && aborted(ctl))) {
                         ok = false;
                         break;
@@ -1361,19 +1485,78 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             }
             const int64_t k = s_k[s];
             if (k >= ntiles) {
-                if (r == 0) mbar_arrive(&folded[s]);
+                if (FX ? lane == 0 : r == 0) mbar_arrive(&folded[s]);
                 return;
             }
             const int nt = row_count(s, r);
+            T run[R];
+            if (nt == R) row_load(run, bufs + (size_t)s * TILE_BYTES, r);
             P tot = M::empty();
-            if (nt == R) {
-                T run[R];
-                row_load(run, bufs + (size_t)s * TILE_BYTES, r);
-                tot = M::lift(row_fold<M>(run));
-            } else if (nt > 0) {
+            if (nt != R && nt > 0) {
                 const T* src = x + row_off(s, r);
                 for (int i = 0; i < nt; ++i) tot = M::combine(tot, M::lift(src[i]));
             }
+            if constexpr (FX) {
+                // Row totals in wide fixed point; their warp scans go ahead,
+                // and the flags written beside the warp totals decide after
+                // the one barrier whether the tile takes the FP64 path
+                // instead (a row with an infinity or a NaN, or with only
+                // zeros and subnormals).
+                const int pb = j & 1;
+                int fm = 1;
+                Fx rt = fx_zero();
+                if (nt == R) {
+                    rt = row_total_fx(run, &fm);
+                } else if (nt > 0) {
+                    const uint64_t tb = (uint64_t)__double_as_longlong(tot);
+                    fm = ((tb >> 52) & 0x7FFu) == 0x7FFu ? 0x7FF : 1;
+                    if (fm == 1) rt = fx_of(tot);
+                }
+                const bool sp = fm == 0 || fm == 0x7FF;
+                rt = fx_norm(rt, 54);
+                Fx inc = rt;
+#pragma unroll
+                for (int d = 1; d < kWarp; d <<= 1) {
+                    const Fx o = fx_shfl_up(inc, d);
+                    if (lane >= d) inc = fx_add(o, inc);
+                }
+                Fx lane_excl = fx_shfl_up(inc, 1);
+                if (lane == 0) lane_excl = fx_zero();
+                const bool wsp = __any_sync(kFull, sp);
+                if (lane == kWarp - 1) {
+                    fwt_fx[pb][fw] = inc;
+                    s_wsp[pb][fw] = wsp;
+                }
+                group_sync(1, ROWS);
+                bool tsp = false;
+#pragma unroll
+                for (int w = 0; w < ROWS / 32; ++w) tsp |= s_wsp[pb][w] != 0;
+                if (!tsp) {
+                    // the warp totals scanned across lanes 0..7
+                    Fx wv = lane < ROWS / 32 ? fwt_fx[pb][lane] : fx_zero();
+#pragma unroll
+                    for (int d = 1; d < ROWS / 32; d <<= 1) {
+                        const Fx o = fx_shfl_up(wv, d);
+                        if (lane >= d) wv = fx_add(o, wv);
+                    }
+                    const Fx base = fx_shfl_idx(wv, fw == 0 ? 0 : fw - 1);
+                    const Fx agg = fx_shfl_idx(wv, ROWS / 32 - 1);
+                    *reinterpret_cast<Fx*>(rowpre_at(s, r)) = fw == 0 ? lane_excl : fx_add(base, lane_excl);  // |a| < 2^62
+                    if (r == 0) {
+                        // published at once: other blocks' look-backs wait for it
+                        const P aggd = fx_to_double(agg);
+                        s_agg[s] = aggd;
+                        s_special[s] = 0;
+                        if (s_t[s] != tiles_per_line - 1 && k != ctl.skip_tile)
+                            publish(ts, k, kStatusAggregate, aggd, ctl.epoch);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&folded[s]);
+                    continue;
+                }
+                if (r == 0) s_special[s] = 1;
+            }
+            if (nt == R) tot = M::lift(row_fold<M>(run));
             const P inc = warp_inclusive_scan<M>(tot, lane);
             P lane_excl = shfl_up_any(inc, 1);
             if (lane == 0) lane_excl = M::empty();
@@ -1392,9 +1575,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 s_agg[s] = agg;
                 if (s_t[s] != tiles_per_line - 1 && k != ctl.skip_tile) publish(ts, k, kStatusAggregate, agg, ctl.epoch);
             }
-            rowpre[(size_t)s * ROWS + r] = M::combine(base, lane_excl);
+            *reinterpret_cast<P*>(rowpre_at(s, r)) = M::combine(base, lane_excl);
             group_sync(1, ROWS);  // every row prefix written; fwt free again
-            if (r == 0) mbar_arrive(&folded[s]);
+            if (FX ? lane == 0 : r == 0) mbar_arrive(&folded[s]);
         }
     }
 
@@ -1411,8 +1594,17 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             }
             const int64_t k = s_k[s];
             if (k >= ntiles) return;
-            const P from = M::combine(s_pre[s], rowpre[(size_t)s * ROWS + r]);
             const int nt = row_count(s, r);
+            P rp;
+            if constexpr (FX) {
+                const Fx rpx = *reinterpret_cast<const Fx*>(rowpre_at(s, r));
+                // (row 0: nothing before it in the tile, the identity -0)
+                rp = s_special[s] ? *reinterpret_cast<const P*>(rowpre_at(s, r))
+                                  : (r == 0 ? M::empty() : fx_to_double(rpx));
+            } else {
+                rp = *reinterpret_cast<const P*>(rowpre_at(s, r));
+            }
+            const P from = M::combine(s_pre[s], rp);
             if (nt == R) {
                 T run[R];
                 row_load(run, bufs + (size_t)s * TILE_BYTES, r);
@@ -1527,7 +1719,7 @@ template <class T, class M>
 int tma_blocks_per_sm(int device) {
     static std::atomic<int> cache[64];
     auto kernel = k_scan_tma<T, M>;
-    constexpr int smem = ws_smem_bytes<typename M::P>();
+    constexpr int smem = ws_smem_bytes<T, M>();
     if (device >= 0 && device < 64) {
         const int v = cache[device].load(std::memory_order_relaxed);
         if (v > 0) return v;
@@ -1574,7 +1766,7 @@ ak_status launch_tma(const ScanCall& c, const ScanPlan& p) {
     // fresh counter, error word and records (correct under CUDA graph replay)
     cudaError_t e = cudaMemsetAsync(ws, 0, p.tma_ws_bytes, c.stream);
     if (e != cudaSuccess) return cuda_fail(e);
-    k_scan_tma<T, M><<<(unsigned)grid, kWsThreads, ws_smem_bytes<typename M::P>(), c.stream>>>(
+    k_scan_tma<T, M><<<(unsigned)grid, kWsThreads, ws_smem_bytes<T, M>(), c.stream>>>(
         tin, static_cast<const T*>(c.src), static_cast<T*>(c.dst), c.len, rows_full, p.tma_tiles_per_line,
         p.tma_tiles, ts, ctl, c.has_init, init, c.exclusive);
     ak_status s = check_launch();
@@ -1605,9 +1797,9 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
         return AK_ERR_UNSUPPORTED;
     } else {
         if (p.block != BLOCK || p.items != ITEMS) return AK_ERR_UNSUPPORTED;
-        if constexpr (std::is_same_v<In, Acc> && std::is_same_v<Acc, Out> &&
-                      (std::is_same_v<Acc, float> || std::is_same_v<Acc, int32_t> || std::is_same_v<Acc, int64_t>) &&
-                      std::is_same_v<typename M::P, Acc>) {
+        if constexpr (std::is_same_v<In, Acc> && std::is_same_v<Acc, Out> && std::is_same_v<typename M::P, Acc> &&
+                      (std::is_same_v<Acc, float> || std::is_same_v<Acc, int32_t> || std::is_same_v<Acc, int64_t> ||
+                       (std::is_same_v<Acc, double> && std::is_same_v<typename M::op, OpAdd>))) {
             if (p.kind == 0 && p.tma) {
                 const ak_status st = launch_tma<Acc, M>(c, p);
                 if (st != AK_ERR_UNSUPPORTED) return st;
@@ -1696,12 +1888,13 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
 
 // The scan plan from the accumulator and partial sizes: kernel kind, run
 // length and block, tile counts and workspace. tma_type: the element type
-// may take the TMA tile scan (one 4- or 8-byte type throughout, f32 / i32 /
-// i64 with a neutral element: f64 additions run on the FP64 pipe, the matrix
-// product spends more operator work per byte and Optional partials more per
-// combine; those run faster as super-tiles, whose blocks carry more warps per
-// SM); it then also needs rows of 128 bytes, several tiles per line, and
-// lines that start on a row boundary unless there is only one.
+// may take the TMA tile scan (one 4- or 8-byte type throughout: f32 / i32 /
+// i64 with a neutral element, and f64 sums, whose folds run in fixed point;
+// the matrix product spends more operator work per byte and Optional
+// partials more per combine, and those run faster on kernels whose blocks
+// carry more warps per SM); it then also needs rows of 128 bytes, several
+// tiles per line, and lines that start on a row boundary unless there is
+// only one.
 // Single lines not on the TMA scan take the reduce-then-scan in three
 // launches at any length: on GB300 it beat the single-pass super-tile scan
 // at every size measured, even where the second read misses L2 (1e8 f64:

@@ -241,6 +241,28 @@ def test_f64_scan_special_values():
     assert_close_f32(y[: n - 100], want[: n - 100], np.cumsum(np.abs(x[: n - 100])), rel=F64_REL)
 
 
+@pytest.mark.parametrize("exclusive", [False, True])
+def test_f64_scan_magnitude_jumps(exclusive):
+    # f64 sums on the TMA scan keep row prefixes in wide fixed point and scan
+    # each row with FP64 additions, some of them backwards from the next
+    # row's prefix; magnitudes that jump by 2^20 .. 2^60 inside a row, a warp
+    # of rows or a tile, and zero-mean data whose prefix keeps returning near
+    # zero, must all stay within the tolerance of the mass before each output
+    n = 4096 * 50 + 5
+    e = np.zeros(n, dtype=np.int64)
+    e[np.arange(n) % 16 >= 8] = 20              # second half of every row 2^20 larger
+    e[(np.arange(n) // 16) % 32 == 31] += 40    # the last row of every warp of rows larger again
+    e[(np.arange(n) // 4096) % 3 == 2] -= 300   # every third tile tiny
+    x = np.ldexp(synth.normal_f64(n, stream=88), e)
+    x[: 4096 * 2] = synth.normal_f64(4096 * 2, stream=89)  # zero-mean start, prefix near 0
+    init = 0.25 if exclusive else None
+    y = ak.ak_accumulate(dev_of("f64", x), init=init, exclusive=exclusive).cpu().numpy()
+    want = oracle.scan(x, "f64", init=init, exclusive=exclusive)
+    a = np.abs(x)
+    mass = (np.concatenate([[0.0], np.cumsum(a)[:-1]]) if exclusive else np.cumsum(a)) + abs(init or 0.0)
+    assert_close_f32(y, want, mass, rel=F64_REL)
+
+
 def test_tma_unaligned_views_fall_back():
     n = 8192 * 4 + 3
     x = gen("f32", n + 1, stream=84, dist="normal")
