@@ -246,6 +246,29 @@ def _time_sustained(fns, rounds, torch):
     return e0.elapsed_time(e1) * 1e3 / (rounds * len(fns)), "loop"
 
 
+def _host_latency_c(n=10**6, reps=300):
+    """The host-result sum timed in C through the C ABI (bench_host_latency.c,
+    built here against the in-tree libak.so): no binding in the timed call.
+    Returns its JSON record, or {"unavailable": why}."""
+    root = os.path.dirname(os.path.abspath(__file__))
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    libdir = os.path.join(root, "mapreduce_prefix_scan_gb300", "_build")
+    exe = os.path.join(libdir, "bench_host_latency")
+    cmd = ["gcc", "-O2", "-std=c11", "-o", exe, os.path.join(root, "bench_host_latency.c"),
+           "-I", os.path.join(root, "include"), "-I", os.path.join(cuda, "include"), "-L", libdir, "-lak",
+           "-L", os.path.join(cuda, "lib64"), "-lcudart", f"-Wl,-rpath,{libdir}", f"-Wl,-rpath,{cuda}/lib64"]
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=120)
+        if r.returncode != 0:
+            return {"unavailable": "build failed: " + r.stderr.strip().splitlines()[-1][:200]}
+        r = subprocess.run([exe, str(n), str(reps)], capture_output=True, text=True, timeout=120)
+        if r.returncode != 0:
+            return {"unavailable": "run failed: " + (r.stderr.strip() or str(r.returncode))[:200]}
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # noqa: BLE001 -- report, do not fail the bench
+        return {"unavailable": repr(e)[:200]}
+
+
 def _configs(ak, torch, dev, peak, flush_buf, reps):
     """Per-workload kernel numbers: one call after an L2 flush (`us_median`,
     `us_min`, and the GB/s and roofline fraction from the median), and the
@@ -289,6 +312,7 @@ def _configs(ak, torch, dev, peak, flush_buf, reps):
                                                                  D["f32"], href(hinit), 1, None, href(hres),
                                                                  ws.data_ptr(), ws.numel(), None, sp)),
         x, 4 * 10**6 + 4, host_sync=True)
+    out["sum_f32_1e6_host_c"] = _host_latency_c()
     rec("sum_i32_1e6_device", lambda a: (lambda: ak.ak_reduce(a, dst=ri, workspace=ws)), xi, 4 * 10**6 + 4)
     del x, xi
     # strided dims=2 reductions

@@ -142,6 +142,8 @@ struct ReduceCall {
     Value16 init;  // accumulator value (valid when mode == AK_STORE_INIT)
     void* dst;     // device output element, or NULL when `bare` is used
     void* bare;    // device slot for the bare partial result (host finish), or NULL
+    void* host_flag = nullptr;  // with `bare` in mapped host memory: the word set to host_seq after it
+    uint64_t host_seq = 0;
     void* ws;
     size_t ws_bytes;
     int target_blocks;

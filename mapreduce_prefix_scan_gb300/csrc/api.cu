@@ -177,6 +177,25 @@ static ak_status sync_and_check(cudaStream_t s) {
     return e == cudaSuccess ? AK_OK : cuda_fail(e);
 }
 
+// Byte offset of the flag word in a host-result slot (after the bare partial).
+constexpr size_t kSlotFlagOff = 32;
+
+// Waits until the host-result slot's flag word holds seq: polled for up to
+// about 200 us (the result lands before the grid has retired and before the
+// stream would report completion), then a stream synchronization, which also
+// reports any error of the stream.
+static ak_status wait_slot(const unsigned char* slot, uint64_t seq, cudaStream_t s) {
+    const uint64_t* flag = reinterpret_cast<const uint64_t*>(slot + kSlotFlagOff);
+    const auto t0 = std::chrono::steady_clock::now();
+    for (int i = 1;; ++i) {
+        if (__atomic_load_n(flag, __ATOMIC_ACQUIRE) == seq) return AK_OK;
+        if ((i & 1023) == 0 && std::chrono::steady_clock::now() - t0 > std::chrono::microseconds(200)) break;
+    }
+    const ak_status st = sync_and_check(s);
+    if (st != AK_OK) return st;
+    return __atomic_load_n(flag, __ATOMIC_ACQUIRE) == seq ? AK_OK : cuda_fail(cudaErrorUnknown);
+}
+
 }  // namespace ak
 
 using namespace ak;
@@ -239,11 +258,12 @@ extern "C" ak_status ak_reduce_workspace_size(int64_t n, ak_dtype in, ak_dtype a
 }
 
 // A per-thread slot of mapped, pinned host memory for host results: the
-// finishing kernel writes the bare partial straight into it (no copy to
-// enqueue, no staging of a pageable buffer), and the host reads it after the
-// stream synchronizes. Allocated on a thread's first host-result call and
-// kept until the process exits (64 bytes). Null when the allocation fails:
-// the caller then copies through the workspace.
+// finishing kernel writes the bare partial straight into its first 32 bytes
+// (no copy to enqueue, no staging of a pageable buffer), then the call's
+// sequence number into the word at byte 32, which the host polls. Allocated
+// on a thread's first host-result call and kept until the process exits (64
+// bytes). Null when the allocation fails: the caller then copies through
+// the workspace.
 static unsigned char* host_result_slot(void** dev_ptr) {
     struct Slot {
         unsigned char* host = nullptr;
@@ -347,7 +367,12 @@ ak_status ak::reduce_entry(const void* src, const void* src2, int map2, int64_t 
     if (!dst_dev && host_slot) {
         void* slot_dev = nullptr;
         slot = host_result_slot(&slot_dev);
-        if (slot) c.bare = slot_dev;
+        if (slot) {
+            static thread_local uint64_t seq = 0;
+            c.bare = slot_dev;
+            c.host_flag = static_cast<char*>(slot_dev) + kSlotFlagOff;
+            c.host_seq = ++seq;
+        }
     }
     c.ws = ws;
     c.ws_bytes = ws_bytes;
@@ -363,7 +388,7 @@ ak_status ak::reduce_entry(const void* src, const void* src2, int map2, int64_t 
             return sync_and_check(st);
         }
         if (slot) {
-            s = sync_and_check(st);
+            s = wait_slot(slot, c.host_seq, st);
             if (s != AK_OK) return s;
             alignas(16) unsigned char bare[32];
             memcpy(bare, slot, sizeof bare);

@@ -41,6 +41,10 @@ struct StoreSpec {
     Acc init;          // for AK_STORE_INIT
     Out* dst;          // final element (device), or null
     typename M::P* bare;  // bare partial for the host finish, or null
+    // with `bare` in mapped host memory: a word the host polls, set to
+    // `seq` once the partial is there (null: the host synchronizes instead)
+    unsigned long long* flag;
+    unsigned long long seq;
 };
 
 template <class Acc, class Out, class M>
@@ -48,6 +52,10 @@ __device__ __forceinline__ void store_result(const typename M::P& r, const Store
     using Op = typename M::op;
     if (st.bare) {
         *st.bare = r;
+        if (st.flag) {
+            __threadfence_system();  // the partial is visible to the host before the flag
+            *reinterpret_cast<volatile unsigned long long*>(st.flag) = st.seq;
+        }
         return;
     }
     Acc v = M::value(r);
@@ -265,6 +273,8 @@ ak_status launch(const ReduceCall& c, const ReducePlan& plan) {
     memcpy(&st.init, c.init.b, sizeof(Acc));
     st.dst = static_cast<Out*>(c.dst);
     st.bare = static_cast<P*>(c.bare);
+    st.flag = static_cast<unsigned long long*>(c.host_flag);
+    st.seq = c.host_seq;
     P* partials = reinterpret_cast<P*>(static_cast<char*>(c.ws) + plan.partials_off);
     const In* x = static_cast<const In*>(c.src);
     const int g = plan.grid;
@@ -301,6 +311,8 @@ ak_status launch2(const ReduceCall& c, const ReducePlan& plan) {
     memcpy(&st.init, c.init.b, sizeof(Acc));
     st.dst = static_cast<Out*>(c.dst);
     st.bare = static_cast<P*>(c.bare);
+    st.flag = static_cast<unsigned long long*>(c.host_flag);
+    st.seq = c.host_seq;
     P* partials = reinterpret_cast<P*>(static_cast<char*>(c.ws) + plan.partials_off);
     const In* a = static_cast<const In*>(c.src);
     const In* b = static_cast<const In*>(c.src2);
