@@ -949,7 +949,7 @@ __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Ac
 constexpr int kTilesBlock = 1024;  // threads of the one-block tile-prefix scan
 // Up to this many tiles the apply blocks fold the aggregates before them
 // themselves (at most this many reads per block, from L2).
-constexpr int64_t kFusedPrefixTiles = 256;
+constexpr int64_t kFusedPrefixTiles = 2048;
 
 template <class In, class M, int BLOCK, int SEG>
 __global__ void __launch_bounds__(BLOCK) k_scan3_fold(const In* __restrict__ x, int64_t len,
@@ -1030,6 +1030,7 @@ __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Ac
         const int64_t per = (t + BLOCK - 1) / BLOCK;
         const int64_t a0 = min(t, (int64_t)tid * per), a1 = min(t, a0 + per);
         P f = M::empty();
+#pragma unroll 4
         for (int64_t q = a0; q < a1; ++q) f = M::combine(f, agg[q]);
         f = block_reduce_ordered<M, BLOCK>(f, red);
         if (tid == 0) s_pre = M::combine(has_init ? M::lift(init) : M::empty(), f);
