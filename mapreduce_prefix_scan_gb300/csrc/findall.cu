@@ -11,15 +11,16 @@
 //   persistent blocks of 256 threads claim tiles of 256 x E elements (E = 64
 //   bytes, 32 four-byte or 16 eight-byte elements a thread; 16 K / 8 K / 4 K
 //   elements a tile). Phase A of tile k: every thread reads its E
-//   consecutive elements with 32-byte loads, turns them into an E-bit mask
-//   (kept in shared memory) and a count; the block sums the counts and
-//   publishes the tile's aggregate (a line's first tile publishes its
-//   inclusive prefix). Phase B of the tile claimed one round earlier: look
-//   back to the tile's exclusive count (decoupled look-back over the
-//   published records, bounded waits), publish its inclusive count, scan the
-//   thread counts, expand every thread's mask into tile-relative positions in
-//   shared memory, and store the tile's indices with consecutive threads on
-//   consecutive output slots (every warp store covers 256 contiguous bytes).
+//   consecutive elements with 32-byte loads and turns them into an E-bit
+//   mask and a count, kept in registers; a warp scan and one barrier give
+//   every thread its offset in the tile and the tile's aggregate, which is
+//   published at once (the first tile publishes its inclusive prefix).
+//   Phase B of the tile claimed one round earlier: look back to the tile's
+//   exclusive count (decoupled look-back over the published records,
+//   bounded waits), publish its inclusive count, expand every thread's mask
+//   into tile-relative positions in shared memory, and store the tile's
+//   indices with consecutive threads on consecutive pairs of output slots
+//   (16-byte stores: every warp store covers 512 contiguous bytes).
 //
 // The input is read once and never re-read (phase B works from the masks);
 // the output is written once: HBM traffic is n * sizeof(T) + 8 * count bytes.
@@ -57,13 +58,17 @@ __device__ __forceinline__ bool nonzero(T v) {
 }
 
 // Mask bits of the 32 bytes of one load: bit b set when byte b is nonzero.
+// Per word: the top bit of every nonzero byte (the low seven bits plus 0x7F
+// carry into it without crossing bytes, or the byte's own top bit is set),
+// then one multiply gathers the four top bits into bits 28..31 (the partial
+// products land on distinct bits, so nothing carries).
 __device__ __forceinline__ uint32_t byte_mask32(const Raw<32>& r) {
     uint32_t m = 0;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-        // 0xFF in every nonzero byte lane; pick bit b of byte b, gather to 4 bits
-        const uint32_t t = __vcmpne4(r.w[w], 0u) & 0x08040201u;
-        m |= ((t | (t >> 8) | (t >> 16) | (t >> 24)) & 0xFu) << (4 * w);
+        const uint32_t v = r.w[w];
+        const uint32_t top = (((v & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | v) & 0x80808080u;
+        m |= (((top >> 7) * 0x10204080u) >> 28) << (4 * w);
     }
     return m;
 }
@@ -111,9 +116,7 @@ __global__ void __launch_bounds__(kBlock, 3)
     constexpr int E = elems_per_thread<T>();
     constexpr int TILE = tile_elems<T>();
     constexpr int W = kBlock / kWarp;
-    __shared__ uint64_t s_mask[2][kBlock];  // the masks of the two open tiles
-    __shared__ int s_cnt[2][kBlock];
-    __shared__ uint16_t s_pos[TILE];        // tile-relative positions, in order
+    __shared__ uint16_t s_pos[TILE];  // tile-relative positions, in order
     __shared__ int64_t red[W];
     __shared__ int ints[2 * kWarp + 1];
     __shared__ int s_wsum[W];
@@ -122,31 +125,46 @@ __global__ void __launch_bounds__(kBlock, 3)
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
     const uint64_t once = l2_policy_evict_first();
 
+    // the tile claimed one round earlier: its count, and this thread's mask
+    // and offset in it
     int64_t prev = -1, prev_agg = 0;
-    int slot = 0;
+    uint64_t prev_mask = 0;
+    int prev_off = 0;
     while (true) {
         if (tid == 0) s_k = (int64_t)atomicAdd(ctl.counter, 1ull);
-        __syncthreads();
+        __syncthreads();  // s_k; the last round's reads of s_pos and s_wsum are done
         const int64_t k = s_k;
+        uint64_t m = 0;
+        int off = 0;
+        if (k < ntiles) {
+            // ---- phase A of tile k: mask, offset, the tile's aggregate
+            m = thread_mask<T>(x, n, k * TILE + (int64_t)tid * E, once);
+            const int c = __popcll(m);
+            int inc = c;
+#pragma unroll
+            for (int d = 1; d < kWarp; d <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, inc, d);
+                if (lane >= d) inc += o;
+            }
+            if (lane == kWarp - 1) s_wsum[warp] = inc;
+            off = inc - c;
+        }
+        __syncthreads();  // the warp totals
         int64_t agg = 0;
         if (k < ntiles) {
-            // ---- phase A of tile k: masks, counts, the tile's aggregate
-            const uint64_t m = thread_mask<T>(x, n, k * TILE + (int64_t)tid * E, once);
-            s_mask[slot][tid] = m;
-            const int c = __popcll(m);
-            s_cnt[slot][tid] = c;
-            agg = scan::block_reduce_ordered<Count, kBlock>((int64_t)c, red);
-            if (tid == 0) {  // thread 0 holds the block total
-                if (k != ctl.skip_tile) scan::publish(ts, k, k == 0 ? scan::kStatusPrefix : scan::kStatusAggregate,
-                                                      agg, ctl.epoch);
-                s_bc = agg;
+            int tot = 0;
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                const int v = s_wsum[w];
+                off += w < warp ? v : 0;
+                tot += v;
             }
-            __syncthreads();
-            agg = s_bc;
+            agg = tot;
+            if (tid == 0 && k != ctl.skip_tile)
+                scan::publish(ts, k, k == 0 ? scan::kStatusPrefix : scan::kStatusAggregate, agg, ctl.epoch);
         }
         if (prev >= 0) {
             // ---- phase B of tile prev: its exclusive count, then the indices
-            const int pslot = slot ^ 1;
             int64_t base = 0;
             if (prev != 0) {
                 if (!scan::look_back<Count, kBlock>(prev, 0, ts, ctl, red, ints, &base)) {
@@ -157,41 +175,51 @@ __global__ void __launch_bounds__(kBlock, 3)
                     if (prev != ctl.skip_tile) scan::publish(ts, prev, scan::kStatusPrefix, base + prev_agg, ctl.epoch);
                     s_bc = base;
                 }
-                __syncthreads();
-                base = s_bc;
             }
-            // exclusive scan of the thread counts
-            const int c = s_cnt[pslot][tid];
-            int inc = c;
-#pragma unroll
-            for (int d = 1; d < kWarp; d <<= 1) {
-                const int o = __shfl_up_sync(0xffffffffu, inc, d);
-                if (lane >= d) inc += o;
+            // the set bits of this thread's mask, as positions in the tile
+            {
+                int o = prev_off;
+                const int p0 = tid * E;
+                uint32_t lo = (uint32_t)prev_mask;
+                while (lo) {
+                    s_pos[o++] = (uint16_t)(p0 + __ffs((int)lo) - 1);
+                    lo &= lo - 1;
+                }
+                if constexpr (E > 32) {
+                    uint32_t hi = (uint32_t)(prev_mask >> 32);
+                    while (hi) {
+                        s_pos[o++] = (uint16_t)(p0 + 31 + __ffs((int)hi));
+                        hi &= hi - 1;
+                    }
+                }
             }
-            if (lane == kWarp - 1) s_wsum[warp] = inc;
-            __syncthreads();
-            int woff = 0;
-#pragma unroll
-            for (int w = 0; w < W; ++w) woff += w < warp ? s_wsum[w] : 0;
-            int off = woff + inc - c;
-            uint64_t m = s_mask[pslot][tid];
-            while (m) {
-                const int b = __ffsll((long long)m) - 1;
-                s_pos[off++] = (uint16_t)(tid * E + b);
-                m &= m - 1;
-            }
-            __syncthreads();
+            __syncthreads();  // positions written; s_bc
+            if (prev != 0) base = s_bc;
             const int total = (int)prev_agg;
             int64_t* out = idx + base;
             const int64_t first = prev * TILE;
-            for (int j = tid; j < total; j += kBlock) out[j] = first + s_pos[j];
+            // pairs of slots on 16-byte boundaries; a leading or trailing
+            // single slot takes an 8-byte store
+            const int lead = (int)((reinterpret_cast<uintptr_t>(out) >> 3) & 1u) < total
+                                 ? (int)((reinterpret_cast<uintptr_t>(out) >> 3) & 1u)
+                                 : total;
+            const int pairs = (total - lead) / 2;
+            if (tid == 0 && lead) out[0] = first + s_pos[0];
+            for (int q = tid; q < pairs; q += kBlock) {
+                const int j = lead + 2 * q;
+                longlong2 v;
+                v.x = first + s_pos[j];
+                v.y = first + s_pos[j + 1];
+                *reinterpret_cast<longlong2*>(out + j) = v;
+            }
+            if (tid == kBlock - 1 && lead + 2 * pairs < total) out[total - 1] = first + s_pos[total - 1];
             if (prev == ntiles - 1 && tid == 0) *count = base + prev_agg;
-            __syncthreads();  // s_pos, s_wsum and the slot are reused next
         }
         if (k >= ntiles) break;
         prev = k;
         prev_agg = agg;
-        slot ^= 1;
+        prev_mask = m;
+        prev_off = off;
     }
 }
 
