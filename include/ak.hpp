@@ -9,7 +9,9 @@
  * without a neutral element, 16-byte non-commutative partials in paragraph
  * "Alternatives"). The C ABI (ak.h) offers a closed set of operators; this
  * header instantiates the same kernels for the caller's own operator inside
- * the caller's translation unit. Compile that unit with nvcc for sm_103a
+ * the caller's translation unit: the whole-array reduction (reduce), the
+ * reduction over a set of dimensions (reduce_dims) and the scan
+ * (accumulate). Compile that unit with nvcc for sm_103a
  * (-gencode arch=compute_103a,code=sm_103a -std=c++17
  * --expt-relaxed-constexpr) and link it with libak.so, which holds the
  * host-side bookkeeping the launchers share (device properties, call
@@ -40,10 +42,12 @@
 #ifndef AK_HPP
 #define AK_HPP
 
+#include <algorithm>
 #include <type_traits>
 
 #include "ak.h"
 #include "../mapreduce_prefix_scan_gb300/csrc/reduce.cuh"
+#include "../mapreduce_prefix_scan_gb300/csrc/reduce_dims.cuh"
 #include "../mapreduce_prefix_scan_gb300/csrc/scan.cuh"
 
 namespace ak {
@@ -75,6 +79,28 @@ constexpr bool supported() {
 template <class T>
 inline bool size_aligned(const void* p) {
     return reinterpret_cast<uintptr_t>(p) % sizeof(T) == 0;
+}
+
+template <class T>
+__global__ void k_fill(T* dst, int64_t n, T v) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = v;
+}
+
+template <class T>
+inline ak_status fill(T* dst, int64_t n, const T& v, cudaStream_t stream) {
+    const int64_t blocks = std::min<int64_t>((n + 255) / 256, 4096);
+    k_fill<T><<<(unsigned)blocks, 256, 0, stream>>>(dst, n, v);
+    const ak_status s = check_launch();
+    if (s == AK_OK) count_launches(1);
+    return s;
+}
+
+// A built-in element type of T's size: the planners size vectors, partials
+// and workspaces by it (a partial of T never outgrows that of the carrier).
+template <class T>
+constexpr ak_dtype carrier() {
+    return sizeof(T) == 4 ? AK_I32 : (sizeof(T) == 8 ? AK_I64 : AK_MAT2_MODP);
 }
 
 }  // namespace user
@@ -127,6 +153,78 @@ ak_status reduce(const T* src, int64_t n, T* dst, const T* init, void* workspace
     c.ws_bytes = workspace_bytes;
     c.stream = stream;
     return red::launch<T, T, T, Map, M>(c, plan);
+}
+
+// ---------------------------------------------------------------------------
+// reduce_dims: dst[kept index] = op(init?, f(src[...]) over the reduced dims)
+// ---------------------------------------------------------------------------
+//
+// As ak_reduce_dims (ak.h): a column-major array of ndim <= 8 dimensions
+// (shape, element strides or NULL for dense), the dimensions in dims_mask
+// (bit d = dimension d) reduced, the kept ones laid out densely in dst in
+// column-major order; init, when given, is applied once per output,
+// leftmost. Non-commutative operators keep the element order along the
+// reduced dimensions.
+
+template <class T, class Op, class Map = MapIdentity>
+ak_status reduce_dims_workspace_size(int ndim, const int64_t* shape, const int64_t* strides, uint32_t dims_mask,
+                                     size_t* bytes) {
+    static_assert(user::supported<T>(), "T: trivially copyable, 4, 8 or 16 bytes");
+    ak_opts o;
+    ak_opts_default(&o);
+    o.no_neutral = Op::has_identity ? 0 : 1;
+    return ak_reduce_dims_workspace_size(ndim, shape, strides, dims_mask, user::carrier<T>(), user::carrier<T>(), &o,
+                                         bytes);
+}
+
+template <class T, class Op, class Map = MapIdentity>
+ak_status reduce_dims(const T* src, int ndim, const int64_t* shape, const int64_t* strides, uint32_t dims_mask,
+                      T* dst, const T* init, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    static_assert(user::supported<T>(), "T: trivially copyable, 4, 8 or 16 bytes");
+    using M = monoid_of<Op, T>;
+    const ak_dtype dt = user::carrier<T>();
+    if (sizeof(typename M::P) > partial_size(dt, !Op::has_identity)) return AK_ERR_UNSUPPORTED;
+    ak_opts o;
+    ak_opts_default(&o);
+    o.no_neutral = Op::has_identity ? 0 : 1;
+    DimsSetup d;
+    ak_status s = setup_dims(src, ndim, shape, strides, dims_mask, dt, dt, o, &d);
+    if (s != AK_OK) return s;
+    const int64_t nin = d.cn.nout * d.cn.nfold;
+    if ((nin > 0 && !src) || (d.cn.nout > 0 && !dst)) return AK_ERR_INVALID_ARG;
+    if (!user::size_aligned<T>(src) || !user::size_aligned<T>(dst)) return AK_ERR_INVALID_ARG;
+    if (d.cn.nout == 0) return AK_OK;
+    if (d.cn.nfold == 0) {
+        if (init) return user::fill(dst, d.cn.nout, *init, stream);
+        if constexpr (Op::has_identity) return user::fill(dst, d.cn.nout, Op::template identity<T>(), stream);
+        else return AK_ERR_EMPTY_NO_INIT;
+    }
+    if (!workspace || workspace_bytes < d.ws_bytes || reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+        return AK_ERR_WORKSPACE;
+    const ak_store mode = init ? AK_STORE_INIT : AK_STORE_OVERWRITE;
+    if (d.path == 1) {
+        ReduceCall c;
+        memset(&c, 0, sizeof c);
+        c.src = src;
+        c.n = d.cn.nfold;
+        c.mode = mode;
+        if (init) memcpy(c.init.b, init, sizeof(T));
+        c.dst = dst;
+        c.ws = workspace;
+        c.ws_bytes = workspace_bytes;
+        c.stream = stream;
+        return red::launch<T, T, T, Map, M>(c, d.rplan);
+    }
+    DimsCall& c = d.c;
+    c.out = dt;
+    c.mode = mode;
+    memset(c.init.b, 0, sizeof c.init.b);
+    if (init) memcpy(c.init.b, init, sizeof(T));
+    c.dst = dst;
+    c.ws = workspace;
+    c.ws_bytes = workspace_bytes;
+    c.stream = stream;
+    return dims::launch<T, T, T, Map, M>(c, d.dplan);
 }
 
 // ---------------------------------------------------------------------------

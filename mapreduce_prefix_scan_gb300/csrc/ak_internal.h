@@ -204,6 +204,32 @@ struct DimsPlan {
 };
 ak_status plan_dims(const DimsCall& c, const DeviceInfo& dev, DimsPlan* plan);
 ak_status run_reduce_dims(const DimsCall& c, const DimsPlan& plan);
+
+// Merged view of a dims reduction: size-1 dimensions dropped, neighbouring
+// dimensions of the same kind (kept / reduced) merged when the source
+// strides continue each other (always, for a dense array).
+struct Canon {
+    int64_t nout, nfold;
+    int nseg;
+    int64_t ext[8];
+    int64_t st[8];  // source stride (elements) of each merged dimension
+    bool red[8];
+};
+
+// The plan of a dims reduction: its merged view, the kernel call (source,
+// types, geometry; the caller fills in output, operator, store mode, init,
+// destination, workspace and stream), and either the whole-array plan
+// (path 1: every element folds into one output) or the dims kernels' plan.
+struct DimsSetup {
+    Canon cn;
+    DimsCall c;
+    int path;  // 0 strided / rows / general, 1 whole-array
+    ReducePlan rplan;
+    DimsPlan dplan;
+    size_t ws_bytes;
+};
+ak_status setup_dims(const void* src, int ndim, const int64_t* shape, const int64_t* strides, uint32_t mask,
+                     ak_dtype in, ak_dtype acc, const ak_opts& o, DimsSetup* d);
 // Fills R where the reduction is empty (store rules of ak_reduce).
 ak_status run_fill(void* dst, int64_t count, ak_dtype out, const Value16& value, cudaStream_t s);
 

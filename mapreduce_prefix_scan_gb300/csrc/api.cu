@@ -430,17 +430,6 @@ extern "C" ak_status ak_reduce2(const void* src_a, const void* src_b, int64_t n,
 
 namespace {
 
-// Merged view of a dims reduction: size-1 dimensions dropped, neighbouring
-// dimensions of the same kind (kept / reduced) merged when the source
-// strides continue each other (always, for a dense array).
-struct Canon {
-    int64_t nout, nfold;
-    int nseg;
-    int64_t ext[8];
-    int64_t st[8];  // source stride (elements) of each merged dimension
-    bool red[8];
-};
-
 ak_status canonicalize(int ndim, const int64_t* shape, const int64_t* strides, uint32_t mask, Canon* c) {
     if (ndim < 1 || ndim > 8 || !shape) return AK_ERR_INVALID_ARG;
     if (mask >> ndim) return AK_ERR_INVALID_ARG;
@@ -505,16 +494,9 @@ int classify(const Canon& cn, DimsCall* c) {
     return 0;
 }
 
-struct DimsSetup {
-    Canon cn;
-    DimsCall c;
-    int path;  // 0 strided / rows / general, 1 whole-array
-    ReducePlan rplan;
-    DimsPlan dplan;
-    size_t ws_bytes;
-};
+}  // namespace
 
-ak_status setup_dims(const void* src, int ndim, const int64_t* shape, const int64_t* strides, uint32_t mask,
+ak_status ak::setup_dims(const void* src, int ndim, const int64_t* shape, const int64_t* strides, uint32_t mask,
                      ak_dtype in, ak_dtype acc, const ak_opts& o, DimsSetup* d) {
     ak_status s = canonicalize(ndim, shape, strides, mask, &d->cn);
     if (s != AK_OK) return s;
@@ -548,8 +530,6 @@ ak_status setup_dims(const void* src, int ndim, const int64_t* shape, const int6
     }
     return s;
 }
-
-}  // namespace
 
 extern "C" ak_status ak_reduce_dims_workspace_size(int ndim, const int64_t* shape, const int64_t* strides,
                                                    uint32_t dims_mask, ak_dtype in, ak_dtype acc, const ak_opts* opts,

@@ -4,8 +4,9 @@ ABI does not offer, compiled into a caller's own translation unit
 
 * Affine maps mod p, v -> a*v + b, composed left to right: a non-commutative
   operator with 8-byte elements, declared with and without an identity (the
-  second runs on Optional partials). Reduce, inclusive and exclusive scans
-  are bit-exact against the oracle's sequential composition.
+  second runs on Optional partials). Reduce, reductions over dimensions,
+  inclusive and exclusive scans are bit-exact against the oracle's
+  sequential composition (per output slice for the dimensions).
 * UserAdd: float addition declared by the caller, which takes the TMA tile
   scan; within 2^-20 * sum |x| of the f64 oracle.
 """
@@ -38,7 +39,8 @@ def U():
     lib = build.build()
     _abi.load()  # libak.so first: the user library links against it
     deps = [SRC, os.path.join(ROOT, "include", "ak.hpp")] + [
-        os.path.join(ROOT, "mapreduce_prefix_scan_gb300", "csrc", f) for f in ("reduce.cuh", "scan.cuh")]
+        os.path.join(ROOT, "mapreduce_prefix_scan_gb300", "csrc", f)
+        for f in ("reduce.cuh", "reduce_dims.cuh", "scan.cuh", "ak_internal.h")]
     if not os.path.exists(OUT) or os.path.getmtime(OUT) < max(os.path.getmtime(d) for d in deps + [lib]):
         os.makedirs(os.path.dirname(OUT), exist_ok=True)
         libdir = os.path.dirname(lib)
@@ -54,6 +56,9 @@ def U():
     L.user_affine_ws.argtypes = [I64, I32, I32, ctypes.POINTER(SZ)]
     L.user_affine_reduce.argtypes = [Pv, I64, Pv, Pv, I32, Pv, SZ, Pv]
     L.user_affine_scan.argtypes = [Pv, Pv, I64, Pv, I32, I32, Pv, SZ, Pv]
+    PI64 = ctypes.POINTER(I64)
+    L.user_affine_dims_ws.argtypes = [I32, PI64, PI64, ctypes.c_uint32, I32, ctypes.POINTER(SZ)]
+    L.user_affine_dims.argtypes = [Pv, I32, PI64, PI64, ctypes.c_uint32, Pv, Pv, I32, Pv, SZ, Pv]
     L.user_add_ws.argtypes = [I64, I32, ctypes.POINTER(SZ)]
     L.user_add_reduce.argtypes = [Pv, I64, Pv, Pv, SZ, Pv]
     L.user_add_scan.argtypes = [Pv, Pv, I64, I32, Pv, SZ, Pv]
@@ -108,6 +113,64 @@ def test_affine_scan(U, n, no_id, mode):
     assert st == 0
     want = oracle.scan_affine(x, init=init, exclusive=excl)
     assert_exact(y.cpu().numpy().view(np.uint32).reshape(-1, 2), want)
+
+
+# (column-major shape, reduced dims): strided middle / leading / trailing
+# dimensions, several reduced blocks, everything, and a strided view
+DIMS_CASES = [((300, 40, 3), (1,)), ((64, 2048), (1,)), ((2048, 64), (0,)), ((17, 5, 33, 4), (0, 2)),
+              ((1000, 33), (0, 1)), ((3, 70000), (1,)), ((9, 11, 7), (0, 1, 2))]
+
+
+@pytest.mark.parametrize("shape,dims", DIMS_CASES)
+@pytest.mark.parametrize("no_id", [0, 1])
+@pytest.mark.parametrize("with_init", [False, True])
+def test_affine_reduce_dims(U, shape, dims, no_id, with_init):
+    n = int(np.prod(shape))
+    x = _affine(n, 134)
+    xd = torch.from_numpy(x.view(np.int32)).cuda()
+    init = np.array([13, 17], np.uint32) if with_init else None
+    mask = sum(1 << d for d in dims)
+    shp = (ctypes.c_int64 * len(shape))(*shape)
+    b = ctypes.c_size_t()
+    assert U.user_affine_dims_ws(len(shape), shp, None, mask, no_id, ctypes.byref(b)) == 0
+    ws = _ws(b.value)
+    kept = [e for d, e in enumerate(shape) if d not in dims]
+    nout = int(np.prod(kept)) if kept else 1
+    out = torch.empty(2 * nout, dtype=torch.int32, device="cuda")
+    st = U.user_affine_dims(xd.data_ptr(), len(shape), shp, None, mask, out.data_ptr(),
+                            None if init is None else init.ctypes.data, no_id, ws.data_ptr(), ws.numel(), _stream())
+    assert st == 0
+    got = out.cpu().numpy().view(np.uint32).reshape(-1, 2)
+    # the oracle's fold of each output's slice, reduced elements in column-major order
+    arr = x.reshape(tuple(reversed(shape)) + (2,))            # numpy axis a = dim ndim-1-a
+    red_axes = sorted(len(shape) - 1 - d for d in dims)      # highest dimension slowest
+    kept_axes = [a for a in range(len(shape)) if a not in red_axes]
+    moved = np.transpose(arr, kept_axes + red_axes + [len(shape)])
+    moved = moved.reshape(nout, -1, 2)                         # outputs in column-major order of the kept dims
+    for o in range(0, nout, max(1, nout // 64)):              # a sample of the outputs
+        assert list(got[o]) == list(oracle.reduce_affine(np.ascontiguousarray(moved[o]), init=init)), o
+    assert got.shape[0] == nout
+
+
+def test_affine_reduce_dims_strided_view(U):
+    # a column-major 60 x 50 x 4 array viewed with every other column: shape
+    # (60, 25, 4), strides (1, 120, 3000); reduce over dimension 1
+    base = _affine(60 * 50 * 4, 135)
+    xd = torch.from_numpy(base.view(np.int32)).cuda()
+    shape, strides = (60, 25, 4), (1, 120, 3000)
+    shp = (ctypes.c_int64 * 3)(*shape)
+    std = (ctypes.c_int64 * 3)(*strides)
+    b = ctypes.c_size_t()
+    assert U.user_affine_dims_ws(3, shp, std, 2, 0, ctypes.byref(b)) == 0
+    ws = _ws(b.value)
+    out = torch.empty(2 * 60 * 4, dtype=torch.int32, device="cuda")
+    assert U.user_affine_dims(xd.data_ptr(), 3, shp, std, 2, out.data_ptr(), None, 0, ws.data_ptr(), ws.numel(),
+                              _stream()) == 0
+    got = out.cpu().numpy().view(np.uint32).reshape(4, 60, 2)
+    full = base.reshape(4, 50, 60, 2)
+    for k in range(4):
+        for i in (0, 7, 59):
+            assert list(got[k, i]) == list(oracle.reduce_affine(np.ascontiguousarray(full[k, ::2, i])))
 
 
 def test_affine_exclusive_without_init(U):

@@ -8,7 +8,8 @@
 //                   partials).
 //   UserAdd         float addition declared by the caller (commutative,
 //                   identity 0): takes the TMA tile scan.
-// The extern "C" wrappers below are what the test calls through ctypes.
+// The extern "C" wrappers below (reduce, reduce over dimensions, scan) are
+// what the test calls through ctypes.
 #include <cstdint>
 
 #include "ak.hpp"
@@ -96,4 +97,20 @@ extern "C" int user_add_scan(const float* src, float* dst, int64_t n, int exclus
                              void* stream) {
     return ak::accumulate<float, UserAdd>(src, dst, n, nullptr, exclusive != 0, ws, ws_bytes,
                                           static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int user_affine_dims_ws(int ndim, const int64_t* shape, const int64_t* strides, uint32_t mask, int no_id,
+                                   size_t* bytes) {
+    return no_id ? ak::reduce_dims_workspace_size<Affine, AffineComposeNoId>(ndim, shape, strides, mask, bytes)
+                 : ak::reduce_dims_workspace_size<Affine, AffineCompose>(ndim, shape, strides, mask, bytes);
+}
+
+extern "C" int user_affine_dims(const void* src, int ndim, const int64_t* shape, const int64_t* strides, uint32_t mask,
+                                void* dst, const void* init, int no_id, void* ws, size_t ws_bytes, void* stream) {
+    auto x = static_cast<const Affine*>(src);
+    auto y = static_cast<Affine*>(dst);
+    auto i = static_cast<const Affine*>(init);
+    auto s = static_cast<cudaStream_t>(stream);
+    return no_id ? ak::reduce_dims<Affine, AffineComposeNoId>(x, ndim, shape, strides, mask, y, i, ws, ws_bytes, s)
+                 : ak::reduce_dims<Affine, AffineCompose>(x, ndim, shape, strides, mask, y, i, ws, ws_bytes, s);
 }
