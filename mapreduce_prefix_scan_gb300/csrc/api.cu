@@ -3,7 +3,10 @@
 // sizing, empty-input rules and the host-side finish of a host result.
 #include <atomic>
 #include <chrono>
+#include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <random>
 
@@ -170,6 +173,33 @@ static ak_status host_finish(const void* bare, ak_dtype in, ak_dtype acc, ak_dty
             });
         });
     });
+}
+
+// AK_LOG set (and not "0") in the environment: one line per call on stderr
+// naming the path the call takes -- kernel, grid or tile count, dims shape.
+// The variable is read on every call, so it can be switched at run time.
+static bool log_on() {
+    const char* v = getenv("AK_LOG");
+    return v && *v && strcmp(v, "0") != 0;
+}
+
+static void log_call(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    char line[256];
+    vsnprintf(line, sizeof line, fmt, ap);
+    va_end(ap);
+    fprintf(stderr, "[ak] %s\n", line);
+}
+
+static const char* dtype_name(ak_dtype t) {
+    static const char* names[] = {"f32", "f64", "i32", "i64", "bf16", "mat2", "u8"};
+    return (int)t >= 0 && (int)t < 7 ? names[t] : "?";
+}
+
+static const char* op_name(ak_op op) {
+    static const char* names[] = {"add", "mul", "max", "min", "matmul_modp"};
+    return (int)op >= 0 && (int)op < 5 ? names[op] : "?";
 }
 
 static ak_status sync_and_check(cudaStream_t s) {
@@ -378,6 +408,11 @@ ak_status ak::reduce_entry(const void* src, const void* src2, int map2, int64_t 
     c.ws_bytes = ws_bytes;
     c.target_blocks = o.target_blocks;
     c.stream = st;
+    if (log_on())
+        log_call("%s n=%lld in=%s acc=%s op=%s first pass %d block(s)%s, result to %s", src2 ? "reduce2" : "reduce",
+                 (long long)n, dtype_name(in), dtype_name(acc), op_name(op), plan.grid,
+                 plan.grid > 1 ? " + one-block finish" : "",
+                 dst_dev ? "device" : (slot ? "host (mapped slot, polled)" : "host (copy)"));
     s = run_reduce(c, plan);
     if (s != AK_OK) return s;
 
@@ -600,6 +635,23 @@ extern "C" ak_status ak_reduce_dims(const void* src, int ndim, const int64_t* sh
         return s;
     }
     if (!ws || ws_bytes < d.ws_bytes || !aligned(ws, 16)) return AK_ERR_WORKSPACE;
+    if (log_on()) {
+        static const char* shapes[] = {"auto", "thread", "tiled", "columns"};
+        if (d.path == 1)
+            log_call("reduce_dims nout=%lld nfold=%lld in=%s op=%s whole-array reduce, %d block(s)",
+                     (long long)d.cn.nout, (long long)d.cn.nfold, dtype_name(in), op_name(op), d.rplan.grid);
+        else if (d.c.general)
+            log_call("reduce_dims nout=%lld nfold=%lld in=%s op=%s general kernel", (long long)d.cn.nout,
+                     (long long)d.cn.nfold, dtype_name(in), op_name(op));
+        else
+            log_call("reduce_dims nout=%lld nfold=%lld in=%s op=%s %s kernel shape=%s vec=%d tile_out=%d "
+                     "row_groups=%d split=%d%s",
+                     (long long)d.cn.nout, (long long)d.cn.nfold, dtype_name(in), op_name(op),
+                     d.c.inner == 1 ? "rows" : "strided",
+                     d.dplan.shape >= 0 && d.dplan.shape < 4 ? shapes[d.dplan.shape] : "?", d.dplan.vec,
+                     d.dplan.tile_out, d.dplan.row_groups, d.dplan.split,
+                     d.dplan.split > 1 ? (d.dplan.cluster ? " (cluster combine)" : " (second pass)") : "");
+    }
     if (d.path == 1) {
         ReduceCall c;
         c.src = src;
@@ -741,6 +793,17 @@ extern "C" ak_status ak_accumulate(const void* src, void* dst, int ndim, const i
     c.skip_tile = o.debug_skip_publish_tile;
     c.epoch = next_epoch();
     c.stream = static_cast<cudaStream_t>(stream);
+    if (log_on()) {
+        const char* k = p.kind == 1 ? "strided (a thread per column)"
+                        : p.kind == 2 ? "lines (one block per line)"
+                        : p.tma ? "TMA tile ring (super-tiles if the pointers are not 16-byte aligned)"
+                        : p.three ? "three-launch reduce-then-scan"
+                                  : "single-pass super-tiles";
+        log_call("accumulate inner=%lld len=%lld outer=%lld in=%s acc=%s op=%s%s%s: %s, %lld tile(s)",
+                 (long long)inner, (long long)len, (long long)outer, dtype_name(in), dtype_name(acc), op_name(op),
+                 c.exclusive ? " exclusive" : "", c.no_neutral ? " optional partials" : "", k,
+                 (long long)(p.tma ? p.tma_tiles : p.tiles));
+    }
     s = run_scan(c, p);
     if (s != AK_OK || !o.check) return s;
     s = sync_and_check(c.stream);
@@ -803,6 +866,9 @@ extern "C" ak_status ak_findall(const void* src, int64_t n, ak_dtype in, int64_t
     if (!ws || ws_bytes < need || !aligned(ws, 16)) return AK_ERR_WORKSPACE;
     int64_t* count = count_dev ? count_dev : reinterpret_cast<int64_t*>(static_cast<char*>(ws) + count_off);
     const uint64_t epoch = next_epoch();
+    if (log_on())
+        log_call("findall n=%lld in=%s: single pass, %lld tile(s), count to %s", (long long)n, dtype_name(in),
+                 (long long)ntiles, count_host ? "host" : "device");
     s = run_findall(src, n, in, idx, count, ws, ntiles, need, epoch, o.wait_limit_ns, o.debug_skip_publish_tile,
                     o.target_blocks, st);
     if (s != AK_OK) return s;
