@@ -1024,7 +1024,9 @@ __global__ void __launch_bounds__(BLOCK, min_blocks_per_sm<BLOCK, (int)sizeof(Ac
     __shared__ P red[W];
     __shared__ P s_pre;
     griddep_wait();
-    const int64_t t = blockIdx.x;
+    // last tile first: the fold went first to last, so the end of a line
+    // longer than L2 is what its evict_last reads left there
+    const int64_t t = (int64_t)gridDim.x - 1 - blockIdx.x;
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
     if (pre == nullptr) {
         const int64_t per = (t + BLOCK - 1) / BLOCK;
