@@ -373,6 +373,9 @@ def _configs(ak, torch, dev, peak, flush_buf, reps):
              opts=ak.make_opts(no_neutral=True))
     scan_rec("cumsum_dims1_4096x4096_f32", synth.normal_f32(4096 * 4096, 0, 62), (4096, 4096), 8 * 4096 * 4096,
              dim=0)
+    # along the strided dimension (column-major dims=2: 4096 columns walking 4096 rows apart)
+    scan_rec("cumsum_dims2_4096x4096_f32", synth.normal_f32(4096 * 4096, 0, 66), (4096, 4096), 8 * 4096 * 4096,
+             dim=1)
     scan_rec("prefix_matmul_modp_1e7", synth.mat2_modp(10**7, 0, 63), (10**7, 4), 32 * 10**7, op="matmul",
              elem="mat2")
     scan_rec("prefix_matmul_modp_dims1_1024x8192", synth.mat2_modp(1024 * 8192, 0, 64), (8192, 1024, 4),

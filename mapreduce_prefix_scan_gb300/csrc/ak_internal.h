@@ -270,6 +270,9 @@ struct ScanPlan {
     // tile prefixes
     bool three;
     size_t seg_off, agg_off, pre_off;
+    // kind 1: the scanned dimension in `chunks` chunks of chunk_rows rows
+    // (1: one thread per column walks it all); the chunk totals at seg_off
+    int64_t chunks, chunk_rows;
 };
 ak_status plan_scan(int64_t inner, int64_t len, int64_t outer, ak_dtype in, ak_dtype acc, ak_dtype out,
                     ak_op op, bool no_neutral, int target_blocks, int items,

@@ -1685,6 +1685,84 @@ __global__ void __launch_bounds__(256) k_scan_strided(const In* __restrict__ x, 
     }
 }
 
+// Lines along a strided dimension with too few columns to fill the GPU:
+// the scanned dimension is cut into `chunks` chunks of CH rows. The fold
+// (block (column tile, chunk)) folds each column's chunk into part[chunk][col];
+// the apply, chained with programmatic dependent launch, starts each column's
+// chunk from init and the totals of the chunks before it (in order) and
+// scans the chunk again, now from L2, storing as it goes.
+constexpr int64_t kStridedTarget = 1 << 18;  // columns x chunks to aim for (about the resident threads)
+constexpr int64_t kStridedMaxChunks = 1024;
+constexpr int64_t kStridedMinRows = 16;       // rows per chunk at least
+
+template <class In, class M>
+__global__ void __launch_bounds__(256) k_scan_strided_fold(const In* __restrict__ x, int64_t I, int64_t J,
+                                                           int64_t K, int64_t CH, typename M::P* __restrict__ part,
+                                                           uint64_t* error_word) {
+    using P = typename M::P;
+    using Acc = typename M::acc;
+    const int64_t cols = I * K;
+    const int64_t col = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t ch = blockIdx.y;
+    if (col == 0 && ch == 0) *error_word = 0;  // no waits here: the call's status is ok
+    if (col < cols) {
+        const int64_t i = col % I, k = col / I;
+        const In* src = x + i + I * J * k;
+        const int64_t j0 = ch * CH, j1 = min(J, j0 + CH);
+        P a = M::empty();
+        constexpr int U = 4;
+        int64_t j = j0;
+        for (; j + U <= j1; j += U) {
+            In v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) v[u] = src[I * (j + u)];
+#pragma unroll
+            for (int u = 0; u < U; ++u) a = M::combine(a, M::lift(convert<Acc>(v[u])));
+        }
+        for (; j < j1; ++j) a = M::combine(a, M::lift(convert<Acc>(src[I * j])));
+        part[ch * cols + col] = a;
+    }
+    griddep_launch_dependents();
+}
+
+template <class In, class Acc, class Out, class M>
+__global__ void __launch_bounds__(256) k_scan_strided_apply(const In* __restrict__ x, Out* __restrict__ y, int64_t I,
+                                                            int64_t J, int64_t K, int64_t CH,
+                                                            const typename M::P* __restrict__ part, bool has_init,
+                                                            Acc init, bool excl) {
+    using P = typename M::P;
+    griddep_wait();
+    const int64_t cols = I * K;
+    const int64_t col = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t ch = blockIdx.y;
+    if (col >= cols) return;
+    P acc = has_init ? M::lift(init) : M::empty();
+#pragma unroll 8
+    for (int64_t q = 0; q < ch; ++q) acc = M::combine(acc, part[q * cols + col]);
+    const int64_t i = col % I, k = col / I;
+    const In* src = x + i + I * J * k;
+    Out* dst = y + i + I * J * k;
+    const int64_t j0 = ch * CH, j1 = min(J, j0 + CH);
+    constexpr int U = 4;
+    int64_t j = j0;
+    for (; j + U <= j1; j += U) {
+        In v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = src[I * (j + u)];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const P before = acc;
+            acc = M::combine(acc, M::lift(convert<Acc>(v[u])));
+            dst[I * (j + u)] = convert<Out>(M::value(excl ? before : acc));
+        }
+    }
+    for (; j < j1; ++j) {
+        const P before = acc;
+        acc = M::combine(acc, M::lift(convert<Acc>(src[I * j])));
+        dst[I * j] = convert<Out>(M::value(excl ? before : acc));
+    }
+}
+
 // cuTensorMapEncodeTiled from the driver the runtime is using (no link-time
 // dependency on libcuda); null when the driver does not provide it.
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -1785,12 +1863,37 @@ ak_status launch(const ScanCall& c, const ScanPlan& p) {
     if (p.kind == 1) {
         const int64_t cols = c.inner * c.outer;
         const unsigned blocks = (unsigned)((cols + 255) / 256);
-        k_scan_strided<In, Acc, Out, M><<<blocks, 256, 0, c.stream>>>(
-            static_cast<const In*>(c.src), static_cast<Out*>(c.dst), c.inner, c.len, c.outer, c.has_init, init,
-            c.exclusive, static_cast<uint64_t*>(c.ws));
+        if (p.chunks <= 1) {
+            k_scan_strided<In, Acc, Out, M><<<blocks, 256, 0, c.stream>>>(
+                static_cast<const In*>(c.src), static_cast<Out*>(c.dst), c.inner, c.len, c.outer, c.has_init, init,
+                c.exclusive, static_cast<uint64_t*>(c.ws));
+            ak_status s = check_launch();
+            if (s == AK_OK) count_launches(1);
+            return s;
+        }
+        P* part = reinterpret_cast<P*>(static_cast<char*>(c.ws) + p.seg_off);
+        const dim3 grid(blocks, (unsigned)p.chunks);
+        k_scan_strided_fold<In, M><<<grid, 256, 0, c.stream>>>(static_cast<const In*>(c.src), c.inner, c.len,
+                                                               c.outer, p.chunk_rows, part,
+                                                               static_cast<uint64_t*>(c.ws));
         ak_status s = check_launch();
-        if (s == AK_OK) count_launches(1);
-        return s;
+        if (s != AK_OK) return s;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.stream = c.stream;
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(256);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, k_scan_strided_apply<In, Acc, Out, M>,
+                                                 static_cast<const In*>(c.src), static_cast<Out*>(c.dst), c.inner,
+                                                 c.len, c.outer, p.chunk_rows, (const P*)part, c.has_init, init,
+                                                 c.exclusive);
+        if (e != cudaSuccess) return cuda_fail(e);
+        count_launches(2);
+        return AK_OK;
     }
     constexpr int ITEMS = default_items<Acc>();
     constexpr int BLOCK = default_block<Acc>();
@@ -1918,10 +2021,23 @@ inline ak_status plan_sizes(int64_t inner, int64_t len, int64_t outer, size_t as
     p->tma_tiles_per_line = 0;
     p->tma_tiles = 0;
     p->tma_ws_bytes = 0;
+    p->chunks = 1;
+    p->chunk_rows = len;
     if (inner > 1) {
         p->kind = 1;
         p->block = 256;
         p->items = 1;
+        // few columns: cut the scanned dimension into chunks (fold, then apply)
+        const int64_t cols = inner * outer;
+        const int64_t chunks = cols < 1 ? 1
+                                        : std::min<int64_t>((kStridedTarget + cols - 1) / cols,
+                                                            std::min<int64_t>(kStridedMaxChunks, len / kStridedMinRows));
+        if (chunks > 1) {
+            p->chunk_rows = (len + chunks - 1) / chunks;
+            p->chunks = (len + p->chunk_rows - 1) / p->chunk_rows;
+            p->seg_off = kWsHeader;
+            p->ws_bytes = std::max(p->ws_bytes, align_up(kWsHeader + (size_t)p->chunks * (size_t)cols * psz, 256));
+        }
         return AK_OK;
     }
     p->kind = 0;

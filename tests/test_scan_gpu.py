@@ -304,6 +304,29 @@ def test_along_dims(shape, dim):
     assert_exact(y.reshape(-1, 4), oracle.scan(xm, "mat2", shape, dim))
 
 
+@pytest.mark.parametrize("shape,dim", [((4096, 2048), 1), ((64, 3000), 1), ((5, 70_000), 1), ((300, 40, 77), 1)])
+@pytest.mark.parametrize("exclusive", [False, True])
+def test_strided_dims_in_chunks(shape, dim, exclusive):
+    # few columns along a long strided dimension: the dimension is cut into
+    # chunks (fold, then apply from the chunk totals before each chunk)
+    n = int(np.prod(shape))
+    rows = tuple(reversed(shape))
+    x = gen("f32", n, stream=76, dist="normal")
+    y = ak.ak_accumulate(dev_of("f32", x).reshape(rows), dim=dim, init=0.5, exclusive=exclusive).cpu().numpy()
+    want = oracle.scan(x, "f32", shape, dim, init=0.5, exclusive=exclusive)
+    mass = _mass_lines(x.astype(np.float64), shape, dim) + 0.5
+    assert_close_f32(y, want, mass)
+    xi = gen("i64", n, stream=77)
+    o = ak.make_opts(no_neutral=True, exclusive=exclusive)
+    y = ak.ak_accumulate(dev_of("i64", xi).reshape(rows), dim=dim, op="max", init=-3, opts=o).cpu().numpy()
+    assert_exact(y, oracle.scan(xi, "i64", shape, dim, op="max", init=-3, exclusive=exclusive))
+    xm = synth.mat2_modp(n, stream=78)
+    init = synth.mat2_modp(1, stream=79)[0]
+    y = ak.ak_accumulate(dev_of("mat2", xm).reshape(rows + (4,)), dim=dim, op="matmul", elem="mat2", init=init,
+                         exclusive=exclusive).cpu().numpy().view(np.uint32)
+    assert_exact(y.reshape(-1, 4), oracle.scan(xm, "mat2", shape, dim, init=init, exclusive=exclusive))
+
+
 # --------------------------------------------------------------------------
 # bounded waits
 # --------------------------------------------------------------------------
