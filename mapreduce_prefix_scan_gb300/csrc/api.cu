@@ -305,6 +305,8 @@ static unsigned char* host_result_slot(void** dev_ptr) {
         slot.tried = true;
         void* h = nullptr;
         if (cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable) == cudaSuccess) {
+            // a zero flag word: no call's sequence number (they start at 1)
+            memset(h, 0, 64);
             void* d = nullptr;
             if (cudaHostGetDevicePointer(&d, h, 0) == cudaSuccess) {
                 slot.host = static_cast<unsigned char*>(h);
