@@ -53,6 +53,11 @@
  * Errors. Every call returns an ak_status. Arguments are validated before
  *   anything is launched, so invalid calls have no effect on the device.
  *   AK_ERR_CUDA keeps the CUDA error, readable with ak_last_cuda_error().
+ * Logging. With AK_LOG set in the environment (and not "0"), every call
+ *   prints one line to stderr naming the path it takes: the first-pass grid
+ *   of a reduction, the dims kernel with its shape, tile and split, the
+ *   scan kernel with its tile count, findall's tile count. The variable is
+ *   read on every call.
  */
 #ifndef AK_H
 #define AK_H
@@ -168,13 +173,20 @@ uint64_t ak_kernel_launch_count(void);
  *   src        device, n elements of `in` (n == 0 allowed)
  *   dst_dev    device, one element of `out`, or NULL
  *   dst_host   host, one element of `out`, or NULL; when given the call
- *              synchronizes `stream` and returns the result there (with
- *              AK_STORE_FOLD, *dst_host holds R_old on entry, unless dst_dev
- *              is also given, in which case R is the device element). The
- *              last pass writes the bare partial straight into a small
- *              mapped, pinned host slot of the calling thread (64 bytes,
- *              allocated by its first host-result call and kept until the
- *              process exits), and the host finishes it.
+ *              returns only once the result is there (with AK_STORE_FOLD,
+ *              *dst_host holds R_old on entry, unless dst_dev is also
+ *              given, in which case R is the device element). The last
+ *              pass writes the bare partial straight into a small mapped,
+ *              pinned host slot of the calling thread (64 bytes, allocated
+ *              by its first host-result call and kept until the process
+ *              exits), then the call's sequence number beside it after a
+ *              system-scope fence. The host polls that word for about
+ *              200 us, then synchronizes `stream` (which also reports any
+ *              error on it), and finishes the partial. The call may thus
+ *              return before the kernel has retired on the stream; later
+ *              work on the stream is ordered after it as usual. An
+ *              asynchronous error that strikes after the result landed
+ *              surfaces on the next synchronizing call.
  *   At least one of dst_dev / dst_host must be non-NULL.
  * Empty input: AK_STORE_INIT stores init; AK_STORE_FOLD leaves R unchanged;
  *   AK_STORE_OVERWRITE stores the neutral element of op (0 for +, 1 for *,
