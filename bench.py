@@ -654,6 +654,10 @@ def run_profile(case: str):
         x = torch.from_numpy(synth.normal_f32(4096 * 4096, 0, 62)).reshape(4096, 4096).to(dev)
         y = torch.empty_like(x)
         fn = lambda: ak.ak_accumulate(x, dst=y, dim=0)
+    elif case == "scan_strided":  # cumsum along dims=2 of 4096 x 4096 f32: the strided dimension in chunks
+        x = torch.from_numpy(synth.normal_f32(4096 * 4096, 0, 66)).reshape(4096, 4096).to(dev)
+        y = torch.empty_like(x)
+        fn = lambda: ak.ak_accumulate(x, dst=y, dim=1)
     elif case == "scan_lines_mat2":  # prefix products along dims=1 of 1024 x 8192 matrices
         x = torch.from_numpy(synth.mat2_modp(1024 * 8192, 0, 64)).reshape(8192, 1024, 4).to(dev)
         y = torch.empty_like(x)
@@ -696,7 +700,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--small", action="store_true", help="n = 1e6 (quick runs)")
     ap.add_argument("--profile", default=None, help="run a small ncu case: reduce|scan|scan_f32|scan_max|scan_mat2|"
-                    "scan_lines|scan_lines_mat2|findall|findall_small|dims|dims_rows|dims_big")
+                    "scan_lines|scan_lines_mat2|scan_strided|findall|findall_small|dims|dims_rows|dims_big")
     args = ap.parse_args()
     if args.profile:
         run_profile(args.profile)
